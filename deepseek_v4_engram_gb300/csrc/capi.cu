@@ -1,0 +1,430 @@
+// C ABI of the Engram forward path: argument validation, the device error word, tensor maps, and
+// the launch sequence of each entry point. Declared in include/engram.h.
+#include <cstdarg>
+#include <cstdio>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include <cudaTypedefs.h>
+
+#include "../../include/engram.h"
+#include "kernels.h"
+
+namespace engram {
+
+// One error word per device (each device that loads the library has its own copy).
+__device__ uint32_t g_error_word;
+
+namespace {
+
+thread_local char g_msg[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int cuda_fail(cudaError_t e, const char* where) {
+  return fail(ENGRAM_ECUDA, "%s: %s", where, cudaGetErrorString(e));
+}
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+uint32_t* g_err_ptr[kMaxDevices] = {};
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+// Device address of this device's error word (resolved once per device, with it current).
+uint32_t* error_word(cudaError_t* e_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    *e_out = e != cudaSuccess ? e : cudaErrorInvalidDevice;
+    return nullptr;
+  }
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_err_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_error_word);
+    if (e != cudaSuccess) {
+      *e_out = e;
+      return nullptr;
+    }
+    g_err_ptr[dev] = static_cast<uint32_t*>(p);
+  }
+  *e_out = cudaSuccess;
+  return g_err_ptr[dev];
+}
+
+bool aligned(const void* p, size_t n) { return (reinterpret_cast<uintptr_t>(p) % n) == 0; }
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(a), b0 = reinterpret_cast<uintptr_t>(b);
+  return a0 < b0 + nb && b0 < a0 + na;
+}
+
+int check_desc(const engram_desc_t* d) {
+  if (d == nullptr) return fail(ENGRAM_EINVAL, "desc is NULL");
+  if (d->dim <= 0 || d->hc_mult <= 0 || d->n_heads <= 0 || d->head_dim <= 0)
+    return fail(ENGRAM_EINVAL, "dim, hc_mult, n_heads and head_dim must be > 0");
+  if (d->max_ngram_size < 2 || d->max_ngram_size > 64)
+    return fail(ENGRAM_EINVAL, "max_ngram_size must be in [2, 64]");
+  if (d->head_dim % 32 != 0)
+    return fail(ENGRAM_EINVAL, "head_dim must be a multiple of 32 (one e8m0 scale per 32)");
+  if (d->dim % 8 != 0) return fail(ENGRAM_EINVAL, "dim must be a multiple of 8");
+  if (d->num_embeddings <= 0 || d->num_embeddings >= (int64_t(1) << 31))
+    return fail(ENGRAM_EINVAL, "num_embeddings must be in [1, 2^31)");
+  if (!(d->norm_eps >= 0.0f)) return fail(ENGRAM_EINVAL, "norm_eps must be >= 0");
+  const int64_t S = int64_t(d->max_ngram_size - 1) * d->n_heads;
+  if (S * d->head_dim >= (int64_t(1) << 30) || int64_t(d->dim) * (d->hc_mult + 1) >= (1 << 30))
+    return fail(ENGRAM_EINVAL, "projection too large");
+  return ENGRAM_OK;
+}
+
+int check_tables(const engram_tables_t* t) {
+  if (t == nullptr) return fail(ENGRAM_EINVAL, "tables is NULL");
+  if (!t->token_map || !t->multipliers || !t->primes || !t->offsets)
+    return fail(ENGRAM_EINVAL, "a table pointer is NULL");
+  if (t->vocab <= 0 || t->pad_id < 0) return fail(ENGRAM_EINVAL, "vocab must be > 0, pad_id >= 0");
+  if (!aligned(t->token_map, 4) || !aligned(t->multipliers, 8) || !aligned(t->primes, 8) ||
+      !aligned(t->offsets, 8))
+    return fail(ENGRAM_EINVAL, "misaligned table pointer");
+  return ENGRAM_OK;
+}
+
+int n_hash_cols(const engram_desc_t* d) { return (d->max_ngram_size - 1) * d->n_heads; }
+
+// ids may be NULL only when ids_optional (the forward then hashes into its workspace).
+int hash_checks(const engram_desc_t* d, const engram_tables_t* t, const int32_t* tokens,
+                int32_t B, int32_t T, int32_t* cache, int32_t* cache_len, int32_t cap,
+                int32_t* ids, bool ids_optional = false) {
+  int rc = check_desc(d);
+  if (rc) return rc;
+  rc = check_tables(t);
+  if (rc) return rc;
+  if (B < 0 || T < 0 || cap < 0) return fail(ENGRAM_EINVAL, "B, T and capacity must be >= 0");
+  if (int64_t(B) * T * n_hash_cols(d) >= (int64_t(1) << 39))
+    return fail(ENGRAM_EINVAL, "B * T too large");
+  if (B * int64_t(T) == 0) return ENGRAM_OK;
+  if (!tokens || !cache || !cache_len || (!ids && !ids_optional))
+    return fail(ENGRAM_EINVAL, "NULL array");
+  if (!aligned(tokens, 4) || !aligned(cache, 4) || !aligned(cache_len, 4) || !aligned(ids, 4))
+    return fail(ENGRAM_EINVAL, "misaligned int32 array");
+  if (ids && overlaps(ids, size_t(B) * T * n_hash_cols(d) * 4, cache, size_t(B) * cap * 4))
+    return fail(ENGRAM_EINVAL, "hash_ids overlaps cache");
+  return ENGRAM_OK;
+}
+
+HashArgs make_hash_args(const engram_desc_t* d, const engram_tables_t* t, const int32_t* tokens,
+                        int32_t B, int32_t T, int32_t* cache, int32_t* cache_len, int32_t cap,
+                        int32_t* ids, uint32_t* err) {
+  HashArgs h{};
+  h.tokens = tokens;
+  h.B = B;
+  h.T = T;
+  h.cache = cache;
+  h.cache_len = cache_len;
+  h.capacity = cap;
+  h.hash_ids = ids;
+  h.token_map = t->token_map;
+  h.vocab = t->vocab;
+  h.pad_id = t->pad_id;
+  h.multipliers = t->multipliers;
+  h.primes = t->primes;
+  h.offsets = t->offsets;
+  h.n_heads = d->n_heads;
+  h.max_ngram = d->max_ngram_size;
+  h.err = err;
+  return h;
+}
+
+constexpr size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
+
+}  // namespace
+
+bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_t rows,
+                        uint32_t box_inner, uint32_t box_rows) {
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_encode == nullptr) {
+      void* fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || fn == nullptr)
+        return false;
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+  }
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = g_encode(static_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              2, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+}  // namespace engram
+
+using namespace engram;
+
+extern "C" {
+
+ENGRAM_API const char* engram_last_error(void) { return g_msg; }
+
+ENGRAM_API int32_t engram_abi_version(void) { return ENGRAM_ABI_VERSION; }
+
+ENGRAM_API int engram_check_errors(void* stream, uint32_t* bits_out) {
+  g_msg[0] = 0;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return cuda_fail(e, "engram_check_errors: stream");
+  uint32_t* w = error_word(&e);
+  if (!w) return cuda_fail(e, "engram_check_errors: error word");
+  uint32_t bits = 0;
+  if ((e = cudaMemcpyAsync(&bits, w, 4, cudaMemcpyDeviceToHost, st)) != cudaSuccess ||
+      (e = cudaMemsetAsync(w, 0, 4, st)) != cudaSuccess ||
+      (e = cudaStreamSynchronize(st)) != cudaSuccess)
+    return cuda_fail(e, "engram_check_errors: read");
+  if (bits_out) *bits_out = bits;
+  if (bits == 0) return ENGRAM_OK;
+  if (bits == ENGRAM_DEVERR_CACHE_FULL)
+    return fail(ENGRAM_ECAPACITY, "a look-back cache ran out of capacity");
+  return fail(ENGRAM_EDEVICE, "device error word 0x%x (1 token range, 2 cache full, 4 id range, "
+              "8 wait timeout)", bits);
+}
+
+ENGRAM_API int engram_hash(const engram_desc_t* desc, const engram_tables_t* tables,
+                           const int32_t* tokens, int32_t B, int32_t T, int32_t* cache,
+                           int32_t* cache_len, int32_t capacity, int32_t* hash_ids,
+                           void* stream) {
+  g_msg[0] = 0;
+  int rc = hash_checks(desc, tables, tokens, B, T, cache, cache_len, capacity, hash_ids);
+  if (rc) return rc;
+  if (int64_t(B) * T == 0) return ENGRAM_OK;
+  cudaError_t e;
+  uint32_t* err = error_word(&e);
+  if (!err) return cuda_fail(e, "engram_hash");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const HashArgs h = make_hash_args(desc, tables, tokens, B, T, cache, cache_len, capacity,
+                                    hash_ids, err);
+  if ((e = launch_hash(h, st)) != cudaSuccess) return cuda_fail(e, "engram_hash: hash kernel");
+  if ((e = launch_advance_len(cache_len, B, T, capacity, st)) != cudaSuccess)
+    return cuda_fail(e, "engram_hash: length update");
+  return ENGRAM_OK;
+}
+
+ENGRAM_API int engram_embed_rows(const engram_desc_t* desc, const uint8_t* table,
+                                 const uint8_t* scales, const int32_t* ids, int64_t n_ids,
+                                 uint16_t* out, void* stream) {
+  g_msg[0] = 0;
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (n_ids < 0 || n_ids >= (int64_t(1) << 36)) return fail(ENGRAM_EINVAL, "bad n_ids");
+  if (n_ids == 0) return ENGRAM_OK;
+  if (!table || !scales || !ids || !out) return fail(ENGRAM_EINVAL, "NULL array");
+  if (!aligned(table, 16) || !aligned(out, 16) || !aligned(ids, 4))
+    return fail(ENGRAM_EINVAL, "table and out must be 16-byte aligned, ids 4-byte aligned");
+  cudaError_t e;
+  uint32_t* err = error_word(&e);
+  if (!err) return cuda_fail(e, "engram_embed_rows");
+  RowsArgs r{};
+  r.table = table;
+  r.scales = scales;
+  r.ids = ids;
+  r.n_ids = n_ids;
+  r.num_rows = desc->num_embeddings;
+  r.head_dim = desc->head_dim;
+  r.out = out;
+  r.err = err;
+  if ((e = launch_rows(r, static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return cuda_fail(e, "engram_embed_rows");
+  return ENGRAM_OK;
+}
+
+ENGRAM_API int engram_wkv(const uint16_t* a, const uint16_t* w, uint16_t* kv, int64_t M,
+                          int32_t N, int32_t K, void* stream) {
+  g_msg[0] = 0;
+  if (M < 0 || N <= 0 || K <= 0) return fail(ENGRAM_EINVAL, "M must be >= 0, N and K > 0");
+  if (M >= (int64_t(1) << 31)) return fail(ENGRAM_EINVAL, "M too large");
+  if (K % 64 != 0 || N % 32 != 0)
+    return fail(ENGRAM_EUNSUPPORTED, "engram_wkv needs K %% 64 == 0 and N %% 32 == 0");
+  if (M == 0) return ENGRAM_OK;
+  if (!a || !w || !kv) return fail(ENGRAM_EINVAL, "NULL array");
+  if (!aligned(a, 16) || !aligned(w, 16) || !aligned(kv, 16))
+    return fail(ENGRAM_EINVAL, "a, w and kv must be 16-byte aligned");
+  if (overlaps(kv, size_t(M) * N * 2, a, size_t(M) * K * 2) ||
+      overlaps(kv, size_t(M) * N * 2, w, size_t(N) * K * 2))
+    return fail(ENGRAM_EINVAL, "kv overlaps an input");
+  cudaError_t e;
+  uint32_t* err = error_word(&e);
+  if (!err) return cuda_fail(e, "engram_wkv");
+  WkvArgs g{a, w, kv, M, N, K, err};
+  if ((e = launch_wkv(g, static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return cuda_fail(e, "engram_wkv");
+  return ENGRAM_OK;
+}
+
+static int gate_checks(const engram_desc_t* desc, const uint16_t* x, const uint16_t* kv,
+                       const uint16_t* q, const uint16_t* k, uint16_t* out, int64_t M) {
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (M < 0 || M * desc->hc_mult >= (int64_t(1) << 31)) return fail(ENGRAM_EINVAL, "bad M");
+  if (M == 0) return ENGRAM_OK;
+  if (!x || !kv || !q || !k || !out) return fail(ENGRAM_EINVAL, "NULL array");
+  if (!aligned(x, 16) || !aligned(kv, 16) || !aligned(q, 16) || !aligned(k, 16) ||
+      !aligned(out, 16))
+    return fail(ENGRAM_EINVAL, "x, kv, q, k and out must be 16-byte aligned");
+  const size_t xbytes = size_t(M) * desc->hc_mult * desc->dim * 2;
+  if (overlaps(out, xbytes, x, xbytes)) return fail(ENGRAM_EINVAL, "out overlaps x");
+  return ENGRAM_OK;
+}
+
+ENGRAM_API int engram_gate_and_add(const engram_desc_t* desc, const uint16_t* x,
+                                   const uint16_t* kv, const uint16_t* q_weight,
+                                   const uint16_t* k_weight, const uint8_t* token_mask,
+                                   uint16_t* out, float* gate_out, int64_t M, void* stream) {
+  g_msg[0] = 0;
+  int rc = gate_checks(desc, x, kv, q_weight, k_weight, out, M);
+  if (rc || M == 0) return rc;
+  GateArgs g{};
+  g.x = x;
+  g.kv = kv;
+  g.q = q_weight;
+  g.k = k_weight;
+  g.mask = token_mask;
+  g.out = out;
+  g.gate_out = gate_out;
+  g.M = M;
+  g.hc = desc->hc_mult;
+  g.dim = desc->dim;
+  g.eps = desc->norm_eps;
+  g.inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));
+  cudaError_t e = launch_gate(g, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "engram_gate_and_add");
+  return ENGRAM_OK;
+}
+
+ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64_t M) {
+  if (check_desc(desc) != ENGRAM_OK || M < 0) return 0;
+  const size_t S = n_hash_cols(desc);
+  const size_t K = S * desc->head_dim;
+  const size_t N = size_t(desc->dim) * (desc->hc_mult + 1);
+  size_t bytes = round256(size_t(M) * S * 4) + round256(size_t(M) * K * 2);
+  if (!fused_supported(static_cast<int32_t>(K), desc->hc_mult, desc->dim))
+    bytes += round256(size_t(M) * N * 2);
+  return bytes;
+}
+
+ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* tables,
+                              const engram_weights_t* wts, const uint16_t* x,
+                              const int32_t* tokens, int32_t B, int32_t T, int32_t* cache,
+                              int32_t* cache_len, int32_t capacity, const uint8_t* token_mask,
+                              uint16_t* out, int32_t* hash_ids_out, float* gate_out,
+                              uint16_t* kv_out, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  g_msg[0] = 0;
+  int rc = hash_checks(desc, tables, tokens, B, T, cache, cache_len, capacity, hash_ids_out,
+                       /*ids_optional=*/true);
+  if (rc) return rc;
+  const int64_t M = int64_t(B) * T;
+  if (wts == nullptr) return fail(ENGRAM_EINVAL, "weights is NULL");
+  rc = gate_checks(desc, x, wts->wkv, wts->q_weight, wts->k_weight, out, M);
+  if (rc) return rc;
+  if (M == 0) return ENGRAM_OK;
+  if (!wts->table || !wts->scales) return fail(ENGRAM_EINVAL, "NULL table");
+  if (!aligned(wts->table, 16)) return fail(ENGRAM_EINVAL, "table must be 16-byte aligned");
+  if (M >= (int64_t(1) << 31)) return fail(ENGRAM_EINVAL, "B * T too large");
+  const int S = n_hash_cols(desc);
+  const int32_t K = S * desc->head_dim;
+  const int32_t N = desc->dim * (desc->hc_mult + 1);
+  if (K % 64 != 0 || N % 32 != 0)
+    return fail(ENGRAM_EUNSUPPORTED, "needs n_hash_cols * head_dim %% 64 == 0");
+  if (kv_out && !aligned(kv_out, 16)) return fail(ENGRAM_EINVAL, "kv_out must be 16-byte aligned");
+  const size_t need = engram_forward_workspace_size(desc, M);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+    return fail(ENGRAM_EINVAL, "workspace must be >= %zu bytes and 256-byte aligned", need);
+
+  cudaError_t e;
+  uint32_t* err = error_word(&e);
+  if (!err) return cuda_fail(e, "engram_forward");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  int32_t* ids = reinterpret_cast<int32_t*>(ws);
+  ws += round256(size_t(M) * S * 4);
+  if (hash_ids_out) ids = hash_ids_out;
+  uint16_t* rows = reinterpret_cast<uint16_t*>(ws);
+  ws += round256(size_t(M) * K * 2);
+
+  // 1. hash (reads cache_len; the row gather below advances it once the hash has run)
+  const HashArgs h = make_hash_args(desc, tables, tokens, B, T, cache, cache_len, capacity, ids,
+                                    err);
+  if ((e = launch_hash(h, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: hash");
+  // 2. gather + dequantise rows -> A [M, K]
+  RowsArgs r{};
+  r.table = wts->table;
+  r.scales = wts->scales;
+  r.ids = ids;
+  r.n_ids = M * S;
+  r.num_rows = desc->num_embeddings;
+  r.head_dim = desc->head_dim;
+  r.out = rows;
+  r.adv_len = cache_len;
+  r.adv_B = B;
+  r.adv_T = T;
+  r.adv_cap = capacity;
+  r.err = err;
+  if ((e = launch_rows(r, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: rows");
+
+  const float inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));
+  if (fused_supported(K, desc->hc_mult, desc->dim)) {
+    // 3+4. projection with the gate fused into its epilogue
+    FusedArgs f{};
+    f.a = rows;
+    f.w = wts->wkv;
+    f.x = x;
+    f.q = wts->q_weight;
+    f.k = wts->k_weight;
+    f.mask = token_mask;
+    f.out = out;
+    f.gate_out = gate_out;
+    f.kv_out = kv_out;
+    f.M = M;
+    f.K = K;
+    f.hc = desc->hc_mult;
+    f.dim = desc->dim;
+    f.eps = desc->norm_eps;
+    f.inv_sqrt_dim = inv_sqrt_dim;
+    f.err = err;
+    if ((e = launch_fused(f, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: fused");
+    return ENGRAM_OK;
+  }
+  // 3. projection -> kv [M, N]; 4. gate and add
+  uint16_t* kv = kv_out ? kv_out : reinterpret_cast<uint16_t*>(ws);
+  WkvArgs g{rows, wts->wkv, kv, M, N, K, err};
+  if ((e = launch_wkv(g, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: wkv");
+  GateArgs ga{};
+  ga.x = x;
+  ga.kv = kv;
+  ga.q = wts->q_weight;
+  ga.k = wts->k_weight;
+  ga.mask = token_mask;
+  ga.out = out;
+  ga.gate_out = gate_out;
+  ga.M = M;
+  ga.hc = desc->hc_mult;
+  ga.dim = desc->dim;
+  ga.eps = desc->norm_eps;
+  ga.inv_sqrt_dim = inv_sqrt_dim;
+  if ((e = launch_gate(ga, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: gate");
+  return ENGRAM_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Internal launch interface between the C ABI (capi.cu) and the kernel translation units.
+// Host-only declarations; every pointer is a device pointer already validated by capi.cu.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace engram {
+
+struct HashArgs {
+  const int32_t* tokens;     // [B, T]
+  int32_t B, T;
+  int32_t* cache;            // [B, capacity]
+  const int32_t* cache_len;  // [B], read only here
+  int32_t capacity;
+  int32_t* hash_ids;         // [B, T, S]
+  const int32_t* token_map;
+  int32_t vocab, pad_id;
+  const uint64_t* multipliers;  // [max_ngram]
+  const uint64_t* primes;       // [S]
+  const int64_t* offsets;       // [S]
+  int32_t n_heads, max_ngram;
+  uint32_t* err;
+};
+
+struct RowsArgs {
+  const uint8_t* table;   // [rows, hd] e4m3
+  const uint8_t* scales;  // [rows, hd/32] e8m0
+  const int32_t* ids;     // [n_ids]
+  int64_t n_ids;
+  int64_t num_rows;
+  int32_t head_dim;
+  uint16_t* out;          // [n_ids, hd] bf16
+  // Optional: advance cache_len[b] += T for b < adv_B (done by block 0), used by the forward to
+  // fold the cache-length update into a kernel that runs after the hash.
+  int32_t* adv_len;
+  int32_t adv_B, adv_T, adv_cap;
+  uint32_t* err;
+};
+
+struct GateArgs {
+  const uint16_t* x;    // [M, hc, dim]
+  const uint16_t* kv;   // [M, dim*(hc+1)]
+  const uint16_t* q;    // [hc, dim]
+  const uint16_t* k;    // [hc, dim]
+  const uint8_t* mask;  // [M] or null
+  uint16_t* out;        // [M, hc, dim]
+  float* gate_out;      // [M, hc] or null
+  int64_t M;
+  int32_t hc, dim;
+  float eps;
+  float inv_sqrt_dim;
+};
+
+struct WkvArgs {
+  const uint16_t* a;  // [M, K]
+  const uint16_t* w;  // [N, K]
+  uint16_t* kv;       // [M, N]
+  int64_t M;
+  int32_t N, K;
+  uint32_t* err;
+};
+
+struct FusedArgs {
+  const uint16_t* a;      // [M, K] gathered rows (bf16)
+  const uint16_t* w;      // [N, K]
+  const uint16_t* x;      // [M, hc, dim]
+  const uint16_t* q;      // [hc, dim]
+  const uint16_t* k;      // [hc, dim]
+  const uint8_t* mask;    // [M] or null
+  uint16_t* out;          // [M, hc, dim]
+  float* gate_out;        // [M, hc] or null
+  uint16_t* kv_out;       // [M, N] or null
+  int64_t M;
+  int32_t K, hc, dim;
+  float eps, inv_sqrt_dim;
+  uint32_t* err;
+};
+
+cudaError_t launch_hash(const HashArgs& a, cudaStream_t s);
+cudaError_t launch_advance_len(int32_t* cache_len, int32_t B, int32_t T, int32_t cap,
+                               cudaStream_t s);
+cudaError_t launch_rows(const RowsArgs& a, cudaStream_t s);
+cudaError_t launch_gate(const GateArgs& a, cudaStream_t s);
+cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t s);
+bool fused_supported(int32_t K, int32_t hc, int32_t dim);
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s);
+
+// Set by capi.cu before any launch: fetches cuTensorMapEncodeTiled from the driver.
+bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_t rows,
+                        uint32_t box_inner, uint32_t box_rows);
+
+}  // namespace engram

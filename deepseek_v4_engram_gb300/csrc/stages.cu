@@ -1,0 +1,268 @@
+// Memory-bound stages of the Engram forward: the n-gram hash (stage 1), the fp8 row gather and
+// dequantisation (stage 2) and the standalone gate-and-add (stage 4).
+#include "device.cuh"
+#include "kernels.h"
+
+namespace engram {
+
+// ------------------------------------------------------------------------------ stage 1: hash
+// Page "Module engram", stage 1 and struct NgramHashState. One thread per (position, slot).
+// Slot s belongs to n-gram size n = s / n_heads + 2; its window is c_{p-k}, k = 0..n-1, taken
+// from this call's tokens (k <= t), from the cache (earlier calls), or pad_id (before p = 0).
+
+__device__ __forceinline__ int32_t compressed_id(const HashArgs& a, int32_t b, int32_t t,
+                                                 int32_t len0, int32_t k) {
+  if (k <= t) {
+    const int32_t tok = __ldg(a.tokens + static_cast<int64_t>(b) * a.T + (t - k));
+    if (tok < 0 || tok >= a.vocab) {
+      set_error(a.err, kErrTokenRange);
+      return a.pad_id;
+    }
+    return __ldg(a.token_map + tok);
+  }
+  const int32_t q = len0 + t - k;  // an earlier call's position
+  if (q < 0) return a.pad_id;
+  if (q >= a.capacity) {           // never cached (the cache was full): flagged on that call
+    set_error(a.err, kErrCacheCapacity);
+    return a.pad_id;
+  }
+  return a.cache[static_cast<int64_t>(b) * a.capacity + q];
+}
+
+__global__ void __launch_bounds__(256) hash_kernel(HashArgs a) {
+  const int32_t S = (a.max_ngram - 1) * a.n_heads;
+  const int64_t total = static_cast<int64_t>(a.B) * a.T * S;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  const int32_t s = static_cast<int32_t>(i % S);
+  const int64_t bt = i / S;
+  const int32_t t = static_cast<int32_t>(bt % a.T);
+  const int32_t b = static_cast<int32_t>(bt / a.T);
+  const int32_t n = s / a.n_heads + 2;
+  const int32_t len0 = a.cache_len[b];
+
+  uint64_t mix = 0;
+  int32_t c0 = 0;
+  for (int32_t k = 0; k < n; ++k) {
+    const int32_t c = compressed_id(a, b, t, len0, k);
+    if (k == 0) c0 = c;
+    mix ^= static_cast<uint64_t>(static_cast<int64_t>(c)) * __ldg(a.multipliers + k);
+  }
+  const uint64_t P = __ldg(a.primes + s);
+  a.hash_ids[i] = static_cast<int32_t>(static_cast<int64_t>(mix % P) + __ldg(a.offsets + s));
+
+  if (s == 0) {  // one thread per position appends c_p to the cache
+    const int64_t p = static_cast<int64_t>(len0) + t;
+    if (p < a.capacity) {
+      a.cache[static_cast<int64_t>(b) * a.capacity + p] = c0;
+    } else {
+      set_error(a.err, kErrCacheCapacity);
+    }
+  }
+}
+
+__global__ void advance_len_kernel(int32_t* len, int32_t B, int32_t T, int32_t cap) {
+  const int32_t b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B) len[b] = min(len[b] + T, cap);
+}
+
+cudaError_t launch_hash(const HashArgs& a, cudaStream_t st) {
+  const int64_t S = (a.max_ngram - 1) * a.n_heads;
+  const int64_t total = static_cast<int64_t>(a.B) * a.T * S;
+  const int64_t blocks = (total + 255) / 256;
+  hash_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_advance_len(int32_t* len, int32_t B, int32_t T, int32_t cap, cudaStream_t st) {
+  advance_len_kernel<<<(B + 255) / 256, 256, 0, st>>>(len, B, T, cap);
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------------------ stage 2: table rows
+// Page "Module engram", stage 2 / embed_rows / regen_table: value * scale per 32-block, to bf16.
+
+// fp8 e4m3fn code -> f32, from its bit fields: sign, 4-bit exponent (bias 7), 3-bit mantissa;
+// exponent 0 is subnormal (m * 2^-9); S.1111.111 is NaN. Exact.
+__device__ __forceinline__ float e4m3_to_f32(uint32_t c) {
+  const uint32_t sign = (c & 0x80u) << 24;
+  const uint32_t E = (c >> 3) & 0xFu;
+  const uint32_t m = c & 0x7u;
+  if (E == 0xFu && m == 0x7u) return __uint_as_float(sign | 0x7FC00000u);
+  if (E == 0) return __uint_as_float(sign | __float_as_uint(static_cast<float>(m) * 0x1p-9f));
+  return __uint_as_float(sign | ((E + 120u) << 23) | (m << 20));
+}
+
+// e8m0 code -> 2^(code - 127) as f32 (code 0 is the binary32 subnormal 2^-127; 255 is NaN).
+__device__ __forceinline__ float e8m0_to_f32(uint32_t c) {
+  if (c == 255u) return __uint_as_float(0x7FC00000u);
+  if (c == 0u) return __uint_as_float(0x00400000u);
+  return __uint_as_float(c << 23);
+}
+
+// Dequantise 16 fp8 codes (one 16-byte chunk) with one scale into 16 bf16 (two 16-byte words).
+__device__ __forceinline__ void dequant16(const uint4 codes, float scale, uint4& lo, uint4& hi) {
+  const uint32_t w[4] = {codes.x, codes.y, codes.z, codes.w};
+  uint32_t o[8];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float v0 = __fmul_rn(e4m3_to_f32(w[j] & 0xFFu), scale);
+    const float v1 = __fmul_rn(e4m3_to_f32((w[j] >> 8) & 0xFFu), scale);
+    const float v2 = __fmul_rn(e4m3_to_f32((w[j] >> 16) & 0xFFu), scale);
+    const float v3 = __fmul_rn(e4m3_to_f32(w[j] >> 24), scale);
+    o[2 * j] = pack_bf16x2(v0, v1);
+    o[2 * j + 1] = pack_bf16x2(v2, v3);
+  }
+  lo = make_uint4(o[0], o[1], o[2], o[3]);
+  hi = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__global__ void __launch_bounds__(256) rows_kernel(RowsArgs a) {
+  if (a.adv_len != nullptr && blockIdx.x == 0) {
+    for (int32_t b = threadIdx.x; b < a.adv_B; b += blockDim.x)
+      a.adv_len[b] = min(a.adv_len[b] + a.adv_T, a.adv_cap);
+  }
+  const int32_t chunks = a.head_dim / 16;
+  const int64_t total = a.n_ids * chunks;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / chunks;
+    const int32_t c = static_cast<int32_t>(i % chunks);
+    const int32_t id = __ldg(a.ids + r);
+    uint4 lo = make_uint4(0, 0, 0, 0), hi = lo;
+    if (id >= 0 && id < a.num_rows) {
+      const uint4 codes = __ldg(reinterpret_cast<const uint4*>(
+          a.table + static_cast<int64_t>(id) * a.head_dim + c * 16));
+      const uint32_t sc = __ldg(a.scales + static_cast<int64_t>(id) * (a.head_dim / 32) + c / 2);
+      dequant16(codes, e8m0_to_f32(sc), lo, hi);
+    } else {
+      set_error(a.err, kErrIdRange);
+    }
+    uint4* dst = reinterpret_cast<uint4*>(a.out + r * a.head_dim + c * 16);
+    dst[0] = lo;
+    dst[1] = hi;
+  }
+}
+
+cudaError_t launch_rows(const RowsArgs& a, cudaStream_t st) {
+  const int64_t total = a.n_ids * (a.head_dim / 16);
+  int64_t blocks = (total + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > (1 << 20)) blocks = 1 << 20;
+  rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+// -------------------------------------------------------------------- stage 4: gate and add
+// Engram listing, forward after the projection; page "DeepSeek V4.1 · Gate per stream".
+// One block per (token, stream): reduce sum h^2, sum key^2, sum h*w*key over dim (16-byte loads,
+// warp shuffles), form the gate, then write h + gate * value (x re-read from L1/L2).
+
+constexpr int kGateThreads = 256;
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// The gate from the three sums (per (token, stream)); mask false -> 0.
+__device__ __forceinline__ float gate_from_sums(float sh2, float sk2, float shwk, int dim,
+                                                float eps, float inv_sqrt_dim) {
+  const float inv_dim = 1.0f / static_cast<float>(dim);
+  const float rstd = rsqrtf(sh2 * inv_dim + eps) * rsqrtf(sk2 * inv_dim + eps);
+  const float a = shwk * rstd * inv_sqrt_dim;
+  const float z = copysignf(sqrtf(fmaxf(fabsf(a), 1e-6f)), a);
+  return 1.0f / (1.0f + expf(-z));
+}
+
+__global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
+  const int64_t m = blockIdx.x / a.hc;
+  const int32_t s = blockIdx.x % a.hc;
+  const int64_t N = static_cast<int64_t>(a.dim) * (a.hc + 1);
+  const uint16_t* xr = a.x + (m * a.hc + s) * a.dim;
+  const uint16_t* key = a.kv + m * N + static_cast<int64_t>(s) * a.dim;
+  const uint16_t* val = a.kv + m * N + static_cast<int64_t>(a.hc) * a.dim;
+  const uint16_t* qr = a.q + static_cast<int64_t>(s) * a.dim;
+  const uint16_t* kr = a.k + static_cast<int64_t>(s) * a.dim;
+  const int nvec = a.dim / 8;
+
+  float sh2 = 0.f, sk2 = 0.f, shwk = 0.f;
+  for (int v = threadIdx.x; v < nvec; v += kGateThreads) {
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr) + v);
+    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(key) + v);
+    const uint4 qv = __ldg(reinterpret_cast<const uint4*>(qr) + v);
+    const uint4 wv = __ldg(reinterpret_cast<const uint4*>(kr) + v);
+    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ks[4] = {kv.x, kv.y, kv.z, kv.w};
+    const uint32_t qs[4] = {qv.x, qv.y, qv.z, qv.w}, ws[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int sh = half * 16;
+        const float h = bf16_bits_to_f32((xs[j] >> sh) & 0xFFFFu);
+        const float kk = bf16_bits_to_f32((ks[j] >> sh) & 0xFFFFu);
+        const float w = bf16_bits_to_f32((qs[j] >> sh) & 0xFFFFu) *
+                        bf16_bits_to_f32((ws[j] >> sh) & 0xFFFFu);
+        sh2 = fmaf(h, h, sh2);
+        sk2 = fmaf(kk, kk, sk2);
+        shwk = fmaf(h * w, kk, shwk);
+      }
+    }
+  }
+  __shared__ float red[3][kGateThreads / 32];
+  __shared__ float gate_s;
+  sh2 = warp_sum(sh2);
+  sk2 = warp_sum(sk2);
+  shwk = warp_sum(shwk);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    red[0][warp] = sh2;
+    red[1][warp] = sk2;
+    red[2][warp] = shwk;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    float r0 = lane < kGateThreads / 32 ? red[0][lane] : 0.f;
+    float r1 = lane < kGateThreads / 32 ? red[1][lane] : 0.f;
+    float r2 = lane < kGateThreads / 32 ? red[2][lane] : 0.f;
+    r0 = warp_sum(r0);
+    r1 = warp_sum(r1);
+    r2 = warp_sum(r2);
+    if (lane == 0) {
+      const bool keep = a.mask == nullptr || a.mask[m] != 0;
+      const float g = keep ? gate_from_sums(r0, r1, r2, a.dim, a.eps, a.inv_sqrt_dim) : 0.f;
+      gate_s = g;
+      if (a.gate_out) a.gate_out[m * a.hc + s] = g;
+    }
+  }
+  __syncthreads();
+  const float g = gate_s;
+  const bool keep = a.mask == nullptr || a.mask[m] != 0;
+  uint16_t* orow = a.out + (m * a.hc + s) * a.dim;
+  for (int v = threadIdx.x; v < nvec; v += kGateThreads) {
+    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr) + v);
+    if (!keep) {
+      reinterpret_cast<uint4*>(orow)[v] = xv;
+      continue;
+    }
+    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(val) + v);
+    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, vs[4] = {vv.x, vv.y, vv.z, vv.w};
+    uint32_t o[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float h0 = bf16_bits_to_f32(xs[j] & 0xFFFFu), h1 = bf16_bits_to_f32(xs[j] >> 16);
+      const float v0 = bf16_bits_to_f32(vs[j] & 0xFFFFu), v1 = bf16_bits_to_f32(vs[j] >> 16);
+      o[j] = pack_bf16x2(fmaf(g, v0, h0), fmaf(g, v1, h1));
+    }
+    reinterpret_cast<uint4*>(orow)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+
+cudaError_t launch_gate(const GateArgs& a, cudaStream_t st) {
+  const int64_t blocks = a.M * a.hc;
+  gate_kernel<<<static_cast<unsigned>(blocks), kGateThreads, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace engram

@@ -1,0 +1,212 @@
+/*
+ * engram.h - C ABI of the GB300 (sm_103a) Engram forward path of DeepSeek V4.1.
+ *
+ * The path has four stages (page "Module engram", CPU reference, stage list 1-4):
+ *   1. hash        token ids -> 24 table-row ids per position, through an n-gram hash whose
+ *                  look-back cache spans calls (prefill then decode);
+ *   2. embed_rows  gather those rows from an fp8 e4m3 table and dequantise them by e8m0 block
+ *                  scales to bf16;
+ *   3. wkv         one bf16 projection [24 * head_dim] -> [dim * (hc_mult + 1)], f32 accumulate,
+ *                  bf16 output: hc_mult keys (one per residual stream) and one shared value;
+ *   4. gate_and_add  per (token, stream): a normalised dot of the stream with its key, weighted by
+ *                  q_weight * k_weight, a signed-sqrt sigmoid gate, and stream + gate * value
+ *                  rounded to bf16.
+ * Each stage has its own entry point; engram_forward runs all four.
+ *
+ * Conventions for every entry point:
+ *  - All array pointers are DEVICE pointers owned by the caller; the library allocates no device
+ *    memory on these calls. Scratch memory is caller-provided (engram_forward_workspace_size).
+ *  - Arrays are dense, row-major, contiguous. bf16 values travel as uint16_t bit patterns, fp8
+ *    e4m3fn and e8m0 as uint8_t. Every array pointer must be 16-byte aligned.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream). Work is enqueued
+ *    asynchronously; a return of ENGRAM_OK means "validated and launched", not "finished".
+ *  - Return value: an engram_status. Arguments are validated on the host before anything is
+ *    launched: a bad argument returns ENGRAM_EINVAL (or ENGRAM_EUNSUPPORTED for a shape the
+ *    kernels do not cover) and launches nothing. Problems that only the device can see (a token
+ *    id outside the vocabulary, a hash id outside the table, a full cache, a kernel wait that gave
+ *    up) set bits in a device error word; engram_check_errors synchronises `stream`, reads the
+ *    word, clears it and returns ENGRAM_EDEVICE (or ENGRAM_ECAPACITY for a full cache).
+ *  - engram_last_error() gives a message for the last non-OK return on the calling thread.
+ *  - Calls that are in flight at the same time on different streams must not share output or
+ *    cache buffers.
+ */
+#ifndef ENGRAM_H_
+#define ENGRAM_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define ENGRAM_API __attribute__((visibility("default")))
+
+typedef enum engram_status {
+  ENGRAM_OK = 0,
+  ENGRAM_EINVAL = 1,       /* bad argument: NULL, negative size, misaligned, aliasing, geometry */
+  ENGRAM_ECAPACITY = 2,    /* a look-back cache ran out of capacity (device-detected)        */
+  ENGRAM_ECUDA = 3,        /* a CUDA runtime call or launch failed                             */
+  ENGRAM_EDEVICE = 4,      /* the device error word was set (see engram_check_errors)         */
+  ENGRAM_EUNSUPPORTED = 5  /* valid, but outside the shapes these kernels implement           */
+} engram_status;
+
+/* Device error word bits, as returned through engram_check_errors(..., &bits). */
+#define ENGRAM_DEVERR_TOKEN_RANGE 1u    /* token id outside [0, vocab)            */
+#define ENGRAM_DEVERR_CACHE_FULL 2u     /* cache_len + T > capacity                */
+#define ENGRAM_DEVERR_ID_RANGE 4u       /* hash id outside [0, num_embeddings)     */
+#define ENGRAM_DEVERR_WAIT_TIMEOUT 8u   /* a bounded in-kernel wait gave up        */
+
+/*
+ * Geometry of one Engram layer (Engram listing, __init__: dim, hc_mult, the layout's n_heads,
+ * max_ngram_size, head_dim and num_embeddings; norm_eps is ModelArgs.norm_eps, whose value the
+ * pages do not give). n_hash_cols = (max_ngram_size - 1) * n_heads rows are fetched per position.
+ * Requirements: all sizes > 0; max_ngram_size >= 2; head_dim % 32 == 0 (one e8m0 scale per 32
+ * elements); dim % 8 == 0; num_embeddings < 2^31; norm_eps >= 0.
+ */
+typedef struct engram_desc {
+  int32_t dim;
+  int32_t hc_mult;
+  int32_t n_heads;
+  int32_t max_ngram_size;
+  int32_t head_dim;
+  int32_t reserved;
+  int64_t num_embeddings;
+  float norm_eps;
+} engram_desc_t;
+
+/*
+ * Hash tables, consumed as given (page "Module engram": the tables paragraph and struct
+ * EngramTables). All pointers are device pointers.
+ *   token_map   int32 [vocab]: tokenizer id -> compressed id (>= 0).
+ *   pad_id      compressed id that fills a window before the sequence start (>= 0).
+ *   multipliers uint64 [max_ngram_size]: multiplier m_k of look-back k (k = 0 is the current
+ *               position); shared by every n-gram size and head.
+ *   primes      uint64 [n_hash_cols]: modulus P_s of slot s = (n - 2) * n_heads + head.
+ *   offsets     int64 [n_hash_cols]: first table row O_s of slot s.
+ * Slot s of position p: id = (mix_n mod P_s) + O_s with mix_n = XOR_{k<n} (c_{p-k} * m_k), all on
+ * unsigned 64-bit words (multiply wraps modulo 2^64).
+ */
+typedef struct engram_tables {
+  const int32_t* token_map;
+  int32_t vocab;
+  int32_t pad_id;
+  const uint64_t* multipliers;
+  const uint64_t* primes;
+  const int64_t* offsets;
+} engram_tables_t;
+
+/*
+ * Parameters of one Engram layer (Engram listing, __init__: embed, wkv, q_weight, k_weight).
+ *   table    uint8 e4m3fn [num_embeddings, head_dim]      (ParallelEngramEmbedding values)
+ *   scales   uint8 e8m0   [num_embeddings, head_dim / 32] (one power-of-two scale per 32 values)
+ *   wkv      bf16 [dim * (hc_mult + 1), n_hash_cols * head_dim]  (Linear weight, [out, in])
+ *   q_weight bf16 [hc_mult, dim];  k_weight bf16 [hc_mult, dim]
+ */
+typedef struct engram_weights {
+  const uint8_t* table;
+  const uint8_t* scales;
+  const uint16_t* wkv;
+  const uint16_t* q_weight;
+  const uint16_t* k_weight;
+} engram_weights_t;
+
+/* Message for the last non-OK status returned on this thread ("" if none). Never NULL. */
+ENGRAM_API const char* engram_last_error(void);
+
+/* Library ABI version (ENGRAM_ABI_VERSION). */
+#define ENGRAM_ABI_VERSION 1
+ENGRAM_API int32_t engram_abi_version(void);
+
+/*
+ * Synchronise `stream`, read and clear the device error word. Returns ENGRAM_OK if it was clear,
+ * ENGRAM_ECAPACITY if only the cache-full bit was set, ENGRAM_EDEVICE otherwise, ENGRAM_ECUDA if
+ * the synchronisation itself failed. `bits_out` (host pointer, may be NULL) receives the word.
+ */
+ENGRAM_API int engram_check_errors(void* stream, uint32_t* bits_out);
+
+/*
+ * Stage 1, the n-gram hash (page "Module engram", stage 1 Hash and struct NgramHashState).
+ *   tokens     int32 [B, T]          token ids of this call (T new positions per sequence).
+ *   cache      int32 [B, capacity]   compressed ids of every position seen so far (in/out).
+ *   cache_len  int32 [B]             positions already in each sequence's cache (in/out: += T).
+ *   hash_ids   int32 [B, T, n_hash_cols]  out.
+ * Position t of sequence b is absolute position p = cache_len[b] + t; its window reaches back
+ * into the cache, so a decode step (T = 1) sees the prefill. Before position 0 the window holds
+ * pad_id. A token outside [0, vocab) is hashed as pad_id and sets ENGRAM_DEVERR_TOKEN_RANGE; a
+ * sequence whose cache would exceed `capacity` sets ENGRAM_DEVERR_CACHE_FULL and the positions
+ * beyond capacity are not cached. B = 0 or T = 0 launches nothing.
+ */
+ENGRAM_API int engram_hash(const engram_desc_t* desc, const engram_tables_t* tables,
+                           const int32_t* tokens, int32_t B, int32_t T, int32_t* cache,
+                           int32_t* cache_len, int32_t capacity, int32_t* hash_ids,
+                           void* stream);
+
+/*
+ * Stage 2, table rows (page "Module engram", stage 2 and function embed_rows; Engram listing,
+ * forward: self.embed(hash_ids)). out[i, d] = bf16(e4m3(table[ids[i], d]) *
+ * 2^(scales[ids[i], d / 32] - 127)); exact for every scale that keeps the product a normal bf16.
+ *   ids  int32 [n_ids];  out bf16 [n_ids, head_dim].
+ * An id outside [0, num_embeddings) writes a zero row and sets ENGRAM_DEVERR_ID_RANGE.
+ */
+ENGRAM_API int engram_embed_rows(const engram_desc_t* desc, const uint8_t* table,
+                                 const uint8_t* scales, const int32_t* ids, int64_t n_ids,
+                                 uint16_t* out, void* stream);
+
+/*
+ * Stage 3, the wkv projection (page "Module engram", stage 3 and function linear_bf16; Engram
+ * listing, forward: self.wkv(...)). kv[m, n] = bf16(sum_k a[m, k] * w[n, k]), f32 accumulation
+ * on the tensor cores, one rounding to bf16.
+ *   a bf16 [M, K];  w bf16 [N, K];  kv bf16 [M, N].
+ * Requires K % 64 == 0 and N % 32 == 0 (else ENGRAM_EUNSUPPORTED). M = 0 launches nothing.
+ */
+ENGRAM_API int engram_wkv(const uint16_t* a, const uint16_t* w, uint16_t* kv, int64_t M,
+                          int32_t N, int32_t K, void* stream);
+
+/*
+ * Stage 4, gate and add (page "Module engram", function gate_and_add; Engram listing, forward
+ * after the projection; page "DeepSeek V4.1 · Gate per stream", formulas for a_k and g^e_k).
+ * For token m and stream s, with h = x[m, s, :], key = kv[m, s*dim : (s+1)*dim],
+ * value = kv[m, hc*dim : (hc+1)*dim] and w = q_weight[s] * k_weight[s]:
+ *   a = sum(h * w * key) / (sqrt(mean(h^2) + eps) * sqrt(mean(key^2) + eps) * sqrt(dim))
+ *   gate = sigmoid(copysign(sqrt(max(|a|, 1e-6)), a)), or 0 where token_mask[m] == 0
+ *   out[m, s, :] = bf16(h + gate * value)
+ * A masked token's row is written as an exact copy of x.
+ *   x bf16 [M, hc, dim]; kv bf16 [M, dim * (hc + 1)]; q_weight, k_weight bf16 [hc, dim];
+ *   token_mask uint8 [M] (nonzero = keep the gate) or NULL (all kept);
+ *   out bf16 [M, hc, dim] (must not overlap x); gate_out f32 [M, hc] or NULL.
+ */
+ENGRAM_API int engram_gate_and_add(const engram_desc_t* desc, const uint16_t* x,
+                                   const uint16_t* kv, const uint16_t* q_weight,
+                                   const uint16_t* k_weight, const uint8_t* token_mask,
+                                   uint16_t* out, float* gate_out, int64_t M, void* stream);
+
+/* Bytes of scratch engram_forward needs for M = B * T tokens (a multiple of 256). */
+ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64_t M);
+
+/*
+ * The whole Engram forward (Engram listing, forward; page "Module engram", stages 1-4) for B
+ * sequences of T new tokens each: hash with the look-back cache, gather and dequantise rows,
+ * project, gate and add. Arguments as in the stage calls above, plus
+ *   x bf16 [B, T, hc, dim]; token_mask uint8 [B, T] or NULL; out bf16 [B, T, hc, dim];
+ *   hash_ids_out int32 [B, T, n_hash_cols] or NULL; gate_out f32 [B, T, hc] or NULL;
+ *   kv_out bf16 [B, T, dim * (hc + 1)] or NULL (the projection, for inspection; costs traffic);
+ *   workspace: device scratch of at least engram_forward_workspace_size(desc, B * T) bytes,
+ *   256-byte aligned, not shared with a concurrent call.
+ * The projection and the gate run in one tensor-core kernel when the geometry allows it (K % 64
+ * == 0, dim % 256 == 0, hc_mult <= 8, dim / hc_mult a multiple of 16); otherwise as separate
+ * kernels. Either way every step runs on the GPU.
+ */
+ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* tables,
+                              const engram_weights_t* weights, const uint16_t* x,
+                              const int32_t* tokens, int32_t B, int32_t T, int32_t* cache,
+                              int32_t* cache_len, int32_t capacity, const uint8_t* token_mask,
+                              uint16_t* out, int32_t* hash_ids_out, float* gate_out,
+                              uint16_t* kv_out, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ENGRAM_H_ */

@@ -1,0 +1,116 @@
+"""Host-side checks of the C ABI (no GPU): the library loads, exports every declared entry point,
+and rejects bad arguments before touching CUDA."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from deepseek_v4_engram_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_entry_points():
+    names = []
+    for h in os.listdir(os.path.join(ROOT, "include")):
+        if h.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", h)).read()
+            names += re.findall(r"ENGRAM_API\s+[\w\s\*]+?\b(engram_\w+)\s*\(", src)
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = declared_entry_points()
+    assert len(names) >= 9
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(_lib.SIGNATURES), "binding and header disagree"
+    assert lib.engram_abi_version() == 1
+
+
+def desc(**kw):
+    d = dict(dim=256, hc_mult=4, n_heads=8, max_ngram_size=4, head_dim=32, reserved=0,
+             num_embeddings=25874, norm_eps=1e-6)
+    d.update(kw)
+    return _lib.EngramDesc(**d)
+
+
+def test_wkv_validation(lib):
+    assert lib.engram_wkv(None, None, None, 16, 1280, 768, None) == _lib.ENGRAM_EINVAL
+    assert lib.engram_wkv(None, None, None, 16, 1280, 760, None) == _lib.ENGRAM_EUNSUPPORTED
+    assert lib.engram_wkv(None, None, None, -1, 1280, 768, None) == _lib.ENGRAM_EINVAL
+    assert lib.engram_wkv(None, None, None, 0, 1280, 768, None) == _lib.ENGRAM_OK   # empty
+    assert lib.engram_wkv(8, 0x1000000, 0x4000000, 16, 1280, 768, None) == _lib.ENGRAM_EINVAL
+    assert b"aligned" in lib.engram_last_error()
+
+
+@pytest.mark.parametrize("bad", [dict(head_dim=48), dict(dim=0), dict(max_ngram_size=1),
+                                 dict(num_embeddings=1 << 31), dict(norm_eps=-1.0),
+                                 dict(dim=260)])
+def test_desc_validation(lib, bad):
+    d = desc(**bad)
+    assert lib.engram_embed_rows(ctypes.byref(d), 16, 16, 16, 4, 16, None) == _lib.ENGRAM_EINVAL
+    assert lib.engram_forward_workspace_size(ctypes.byref(d), 16) == 0
+
+
+def test_gate_rejects_aliasing_and_misalignment(lib):
+    d = desc()
+    x = 0x10000
+    # out overlapping x
+    rc = lib.engram_gate_and_add(ctypes.byref(d), x, 0x900000, 0x2000, 0x4000, None, x + 256,
+                                 None, 4, None)
+    assert rc == _lib.ENGRAM_EINVAL and b"overlaps" in lib.engram_last_error()
+    rc = lib.engram_gate_and_add(ctypes.byref(d), x + 2, 0x900000, 0x2000, 0x4000, None,
+                                 0x800000, None, 4, None)
+    assert rc == _lib.ENGRAM_EINVAL and b"aligned" in lib.engram_last_error()
+    assert lib.engram_gate_and_add(ctypes.byref(d), None, None, None, None, None, None, None, 0,
+                                   None) == _lib.ENGRAM_OK
+
+
+def test_hash_validation(lib):
+    d = desc()
+    t = _lib.EngramTables(0x1000, 1000, 0, 0x2000, 0x3000, 0x4000)
+    args = [ctypes.byref(d), ctypes.byref(t), 0x5000, 2, 3, 0x6000, 0x7000, 8, 0x8000, None]
+    bad = list(args)
+    bad[3] = -1
+    assert lib.engram_hash(*bad) == _lib.ENGRAM_EINVAL
+    bad = list(args)
+    bad[8] = None
+    assert lib.engram_hash(*bad) == _lib.ENGRAM_EINVAL
+    t2 = _lib.EngramTables(0x1000, 1000, -3, 0x2000, 0x3000, 0x4000)
+    bad = list(args)
+    bad[1] = ctypes.byref(t2)
+    assert lib.engram_hash(*bad) == _lib.ENGRAM_EINVAL
+    # ids overlapping the cache
+    bad = list(args)
+    bad[8] = 0x6000
+    assert lib.engram_hash(*bad) == _lib.ENGRAM_EINVAL
+    bad = list(args)
+    bad[3] = 0
+    assert lib.engram_hash(*bad) == _lib.ENGRAM_OK          # nothing to do
+
+
+def test_forward_workspace_and_validation(lib):
+    d = desc()
+    n16 = lib.engram_forward_workspace_size(ctypes.byref(d), 16)
+    n32 = lib.engram_forward_workspace_size(ctypes.byref(d), 32)
+    assert n16 > 0 and n32 > n16 and n16 % 256 == 0
+    t = _lib.EngramTables(0x1000, 1000, 0, 0x2000, 0x3000, 0x4000)
+    w = _lib.EngramWeights(0x10000, 0x20000, 0x30000, 0x40000, 0x50000)
+    # workspace too small
+    rc = lib.engram_forward(ctypes.byref(d), ctypes.byref(t), ctypes.byref(w), 0x100000, 0x5000,
+                            1, 16, 0x6000, 0x7000, 16, None, 0x900000, None, None, None,
+                            0x1000000, 64, None)
+    assert rc == _lib.ENGRAM_EINVAL and b"workspace" in lib.engram_last_error()
+    # weights missing
+    rc = lib.engram_forward(ctypes.byref(d), ctypes.byref(t), None, 0x100000, 0x5000, 1, 16,
+                            0x6000, 0x7000, 16, None, 0x900000, None, None, None, 0x1000000,
+                            n16, None)
+    assert rc == _lib.ENGRAM_EINVAL

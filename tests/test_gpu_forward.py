@@ -1,0 +1,120 @@
+"""GPU parity of the whole forward (engram_forward) against the oracle.
+
+Three checks per run:
+  1. hash ids bit-exact, and the projection (kv_out) within one bf16 ulp of the oracle's;
+  2. out and gate against the oracle's gate-and-add fed the GPU's own kv: within tolerance
+     everywhere (this isolates the gate from f32-order flips of kv);
+  3. out against the oracle's full forward: every element beyond tolerance must be explained by a
+     value element of kv that differs from the oracle's (within the projection's tolerance).
+"""
+import numpy as np
+import pytest
+import torch
+
+import deepseek_v4_engram_gb300 as eg
+import synth
+from oracle import engram as E
+from oracle.numerics import bf16_to_f64, bf16_ulp
+from tests.helpers import (assert_gate_close, assert_kv_close, assert_out_close, dev, empty_bf16,
+                           host, kv_tolerance, out_violations)
+
+pytestmark = pytest.mark.gpu
+
+FULLISH = synth.Geometry(dim=5120, hc_mult=4, n_heads=8, max_ngram_size=4, head_dim=64,
+                         vocab=129280, n_compressed=100000, prime_floor=1 << 14)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    from tests.gpu_fixtures import DeviceModel
+    return DeviceModel(synth.make_model(synth.TINY, synth.BASE_SEED))
+
+
+@pytest.fixture(scope="module")
+def wide():
+    from tests.gpu_fixtures import DeviceModel
+    return DeviceModel(synth.make_model(FULLISH, synth.BASE_SEED + 9, scale_mode="pow2"))
+
+
+def run_forward(dm, batch, cache=None, length=None, capacity=None):
+    B, T = batch.tokens.shape
+    g = dm.geom
+    if cache is None:
+        cache, length = dm.new_cache(B, capacity or T)
+    out = empty_bf16(B, T, g.hc_mult, g.dim)
+    ids = torch.full((B, T, g.n_hash_cols), -1, dtype=torch.int32, device="cuda")
+    gate = torch.full((B, T, g.hc_mult), float("nan"), device="cuda")
+    kv = empty_bf16(B, T, g.N)
+    ws = dm.workspace(B * T)
+    mask = None if batch.mask is None else dev(batch.mask)
+    eg.engram_forward(dm.desc, dm.tables, dm.weights, dev(batch.x), dev(batch.tokens), cache,
+                      length, mask, out, ws, hash_ids_out=ids, gate_out=gate, kv_out=kv)
+    assert eg.engram_check_errors() == 0
+    return dict(out=host(out), hash_ids=host(ids), gate=host(gate), kv=host(kv),
+                cache=cache, length=length)
+
+
+def check_against_oracle(dm, batch, r, state=None):
+    B, T = batch.tokens.shape
+    g, m = dm.geom, dm.model
+    M = B * T
+    st = state or E.NgramHashState(m.tables.token_map, m.tables.pad_id, m.tables.multipliers,
+                                   m.tables.primes, m.tables.offsets, g.n_heads,
+                                   g.max_ngram_size, B)
+    ref = E.forward(st, m.table, m.scales, m.wkv, m.q, m.k, batch.x, batch.tokens, batch.mask,
+                    m.eps)
+    # 1. integer stages bit-exact, projection within one ulp
+    np.testing.assert_array_equal(r["hash_ids"], ref["hash_ids"])
+    A = ref["rows"].reshape(M, -1)
+    assert_kv_close(r["kv"].reshape(M, -1), ref["kv"].reshape(M, -1), A, m.wkv)
+    # 2. the gate stage alone, on the GPU's own kv
+    mask = None if batch.mask is None else batch.mask.reshape(M)
+    x = batch.x.reshape(M, g.hc_mult, g.dim)
+    o2, g2 = E.gate_and_add(x, r["kv"].reshape(M, -1), m.q, m.k, mask, m.eps)
+    assert_gate_close(r["gate"].reshape(M, -1), g2)
+    value_gpu = r["kv"].reshape(M, -1)[:, g.hc_mult * g.dim:]
+    assert_out_close(r["out"].reshape(M, g.hc_mult, g.dim), o2, value_gpu)
+    # 3. end to end: outliers only where a value element flipped by one ulp
+    assert_gate_close(r["gate"].reshape(M, -1), ref["gate"].reshape(M, -1))
+    value_ref = ref["kv"].reshape(M, -1)[:, g.hc_mult * g.dim:]
+    bad = out_violations(r["out"].reshape(M, g.hc_mult, g.dim), ref["out"].reshape(M, g.hc_mult,
+                                                                                    g.dim), value_ref)
+    if bad.any():
+        vg, vr = bf16_to_f64(value_gpu), bf16_to_f64(value_ref)
+        tol = kv_tolerance(ref["kv"].reshape(M, -1), A, m.wkv)[:, g.hc_mult * g.dim:]
+        flipped = (vg != vr) & (np.abs(vg - vr) <= tol)
+        m_idx, s_idx, d_idx = np.nonzero(bad)
+        assert flipped[m_idx, d_idx].all(), "an output outlier is not explained by a kv flip"
+    if mask is not None:
+        np.testing.assert_array_equal(r["out"].reshape(M, g.hc_mult, g.dim)[~mask], x[~mask])
+    return ref
+
+
+@pytest.mark.parametrize("B,T", [(1, 16), (2, 17), (1, 129), (3, 100)])
+def test_forward_tiny(tiny, B, T):
+    batch = synth.make_batch(tiny.geom, B, T, synth.BASE_SEED + 100 + T)
+    check_against_oracle(tiny, batch, run_forward(tiny, batch))
+
+
+@pytest.mark.parametrize("B,T,mask_frac", [(1, 1, 0.0), (2, 77, 0.0), (1, 300, 0.1),
+                                           (4, 160, 0.1)])
+def test_forward_full_width(wide, B, T, mask_frac):
+    batch = synth.make_batch(wide.geom, B, T, synth.BASE_SEED + 200 + T, x_dist="student_t3",
+                             mask_frac=mask_frac)
+    check_against_oracle(wide, batch, run_forward(wide, batch))
+
+
+def test_prefill_then_decode_equals_one_prefill(wide):
+    # the look-back cache carries across calls: prefill(T) == prefill(T-j) + j decode steps
+    B, T, j = 3, 40, 4
+    batch = synth.make_batch(wide.geom, B, T, synth.BASE_SEED + 300)
+    whole = run_forward(wide, batch)
+    cache, length = wide.new_cache(B, T)
+    head = synth.Batch(batch.tokens[:, :T - j], batch.x[:, :T - j], None)
+    parts = [run_forward(wide, head, cache, length)]
+    for t in range(T - j, T):
+        step = synth.Batch(batch.tokens[:, t:t + 1], batch.x[:, t:t + 1], None)
+        parts.append(run_forward(wide, step, cache, length))
+    for key in ("hash_ids", "out", "kv"):
+        np.testing.assert_array_equal(np.concatenate([p[key] for p in parts], 1), whole[key])
+    np.testing.assert_array_equal(host(length), [T] * B)
