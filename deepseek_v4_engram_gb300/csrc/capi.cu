@@ -145,20 +145,40 @@ constexpr size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
 }  // namespace
 
+namespace {
+bool have_encoder() {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (g_encode == nullptr) {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || fn == nullptr)
+      return false;
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  }
+  return true;
+}
+}  // namespace
+
+bool tensor_map_3d_bf16(void* map_out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                        uint32_t box0, uint32_t box1, uint32_t box2) {
+  if (!have_encoder()) return false;
+  const cuuint64_t dims[3] = {d0, d1, d2};
+  const cuuint64_t strides[2] = {d0 * 2, d0 * d1 * 2};
+  const cuuint32_t box[3] = {box0, box1, box2};
+  const cuuint32_t estr[3] = {1, 1, 1};
+  const CUresult r = g_encode(static_cast<CUtensorMap*>(map_out), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                              3, const_cast<void*>(base), dims, strides, box, estr,
+                              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                              CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_t rows,
                         uint32_t box_inner, uint32_t box_rows) {
-  {
-    std::lock_guard<std::mutex> lock(g_mu);
-    if (g_encode == nullptr) {
-      void* fn = nullptr;
-      cudaDriverEntryPointQueryResult q;
-      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
-                                           cudaEnableDefault, &q) != cudaSuccess ||
-          q != cudaDriverEntryPointSuccess || fn == nullptr)
-        return false;
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-    }
-  }
+  if (!have_encoder()) return false;
   const cuuint64_t dims[2] = {inner, rows};
   const cuuint64_t strides[1] = {inner * 2};
   const cuuint32_t box[2] = {box_inner, box_rows};

@@ -100,6 +100,22 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
 }
 
+// Orders this thread's generic-proxy shared-memory accesses before later async-proxy (TMA)
+// accesses that other threads issue after synchronising with it (e.g. a TMA load that refills a
+// buffer this thread has just read).
+__device__ __forceinline__ void fence_proxy_async_shared() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t saddr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(saddr)
+               : "memory");
+  return v;
+}
+
 // ----------------------------------------------------------------------------------------- TMA
 
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap* map) {
@@ -115,6 +131,16 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
       " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+      : "memory");
+}
+
+// 3-D tiled load (x innermost); same alignment rule for x as tma_load_2d.
+__device__ __forceinline__ void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                            int32_t x, int32_t y, int32_t z) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%3, %4, %5}], [%2];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
 
@@ -181,6 +207,20 @@ __device__ __forceinline__ void tc_wait_ld() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+// tcgen05.wait::ld that also ties the destination registers of the preceding tcgen05.ld, so the
+// compiler cannot schedule any use of them before the wait.
+__device__ __forceinline__ void tc_wait_ld(uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+        "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+        "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]),
+        "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]),
+        "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
+
 // Shared-memory matrix descriptor of a K-major bf16 tile stored with the 128-byte swizzle, as a
 // TMA load with CU_TENSOR_MAP_SWIZZLE_128B writes it: rows of 64 elements (128 B), 8-row groups
 // 1024 B apart. The tile must start on a 1024-byte boundary.
@@ -213,7 +253,7 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 }
 
 __device__ __forceinline__ void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::
+  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::
                    : "memory");
 }
 
@@ -249,6 +289,24 @@ __device__ __forceinline__ float round_bf16(float v) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
+  return v;
+}
+
+// The gate of one (token, stream) from its three sums over dim (Engram listing, forward; page
+// "DeepSeek V4.1 · Gate per stream"): rstd = rsqrt(mean h^2 + eps) * rsqrt(mean key^2 + eps),
+// a = (sum h*w*key) * rstd * dim^-1/2, gate = sigmoid(copysign(sqrt(max(|a|, 1e-6)), a)).
+__device__ __forceinline__ float gate_from_sums(float sh2, float sk2, float shwk, int dim,
+                                                float eps, float inv_sqrt_dim) {
+  const float inv_dim = 1.0f / static_cast<float>(dim);
+  const float rstd = rsqrtf(sh2 * inv_dim + eps) * rsqrtf(sk2 * inv_dim + eps);
+  const float a = shwk * rstd * inv_sqrt_dim;
+  const float z = copysignf(sqrtf(fmaxf(fabsf(a), 1e-6f)), a);
+  return 1.0f / (1.0f + expf(-z));
 }
 
 }  // namespace engram

@@ -87,8 +87,11 @@ cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t s);
 bool fused_supported(int32_t K, int32_t hc, int32_t dim);
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s);
 
-// Set by capi.cu before any launch: fetches cuTensorMapEncodeTiled from the driver.
+// Tensor maps (capi.cu; cuTensorMapEncodeTiled is fetched from the driver on first use).
 bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_t rows,
                         uint32_t box_inner, uint32_t box_rows);
+// 3-D bf16 tensor [d2][d1][d0] (d0 innermost, dense), 128-byte swizzle.
+bool tensor_map_3d_bf16(void* map_out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
+                        uint32_t box0, uint32_t box1, uint32_t box2);
 
 }  // namespace engram

@@ -160,22 +160,6 @@ cudaError_t launch_rows(const RowsArgs& a, cudaStream_t st) {
 
 constexpr int kGateThreads = 256;
 
-__device__ __forceinline__ float warp_sum(float v) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xFFFFFFFFu, v, o);
-  return v;
-}
-
-// The gate from the three sums (per (token, stream)); mask false -> 0.
-__device__ __forceinline__ float gate_from_sums(float sh2, float sk2, float shwk, int dim,
-                                                float eps, float inv_sqrt_dim) {
-  const float inv_dim = 1.0f / static_cast<float>(dim);
-  const float rstd = rsqrtf(sh2 * inv_dim + eps) * rsqrtf(sk2 * inv_dim + eps);
-  const float a = shwk * rstd * inv_sqrt_dim;
-  const float z = copysignf(sqrtf(fmaxf(fabsf(a), 1e-6f)), a);
-  return 1.0f / (1.0f + expf(-z));
-}
-
 __global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
   const int64_t m = blockIdx.x / a.hc;
   const int32_t s = blockIdx.x % a.hc;

@@ -133,7 +133,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
       for (int c = 0; c < kBN / 32; ++c) {
         uint32_t r[32];
         tc_ld_32x32b_x32(tmem_base + lane_base + acc * kBN + c * 32, r);
-        tc_wait_ld();
+        tc_wait_ld(r);
         if (m < M && n0 + c * 32 < N) {
           uint4* dst = reinterpret_cast<uint4*>(kv + m * N + n0 + c * 32);
 #pragma unroll

@@ -28,9 +28,10 @@ __device__ __forceinline__ void mbar_wait_drain(uint64_t* bar, uint32_t parity) 
   }
 }
 
-// Producer side of the stage ring: which stage to fill next, and which loads are in flight so
-// they can be waited for before the CTA exits.
-struct TmaRing {
+// Producer side of a ring of kSlots TMA buffers: which slot to fill next, and which loads are in
+// flight so they can be waited for before the CTA exits.
+template <int kSlots>
+struct TmaRingT {
   uint32_t stage = 0, phase = 0;
   uint32_t issued_mask = 0;
   uint32_t issued_parity = 0;  // bit s: parity of the last load issued into stage s
@@ -41,16 +42,18 @@ struct TmaRing {
   __device__ __forceinline__ void issued() {
     issued_mask |= 1u << stage;
     issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
-    if (++stage == kStages) {
+    if (++stage == kSlots) {
       stage = 0;
       phase ^= 1u;
     }
   }
   // Wait (bounded) until every issued load has landed.
   __device__ __forceinline__ void drain(uint64_t* full) {
-    for (int s = 0; s < kStages; ++s)
+    for (int s = 0; s < kSlots; ++s)
       if (issued_mask & (1u << s)) mbar_wait_drain(&full[s], (issued_parity >> s) & 1u);
   }
 };
+
+using TmaRing = TmaRingT<kStages>;
 
 }  // namespace engram

@@ -4,8 +4,8 @@ Three checks per run:
   1. hash ids bit-exact, and the projection (kv_out) within one bf16 ulp of the oracle's;
   2. out and gate against the oracle's gate-and-add fed the GPU's own kv: within tolerance
      everywhere (this isolates the gate from f32-order flips of kv);
-  3. out against the oracle's full forward: every element beyond tolerance must be explained by a
-     value element of kv that differs from the oracle's (within the projection's tolerance).
+  3. gate and out against the oracle's full forward, allowing on top of the stage tolerances the
+     difference that the GPU's kv (within its own tolerance) causes, as the oracle measures it.
 """
 import numpy as np
 import pytest
@@ -15,8 +15,8 @@ import deepseek_v4_engram_gb300 as eg
 import synth
 from oracle import engram as E
 from oracle.numerics import bf16_to_f64, bf16_ulp
-from tests.helpers import (assert_gate_close, assert_kv_close, assert_out_close, dev, empty_bf16,
-                           host, kv_tolerance, out_violations)
+from tests.helpers import (GATE_ATOL, assert_gate_close, assert_kv_close, assert_out_close, dev,
+                           empty_bf16, host)
 
 pytestmark = pytest.mark.gpu
 
@@ -28,6 +28,17 @@ FULLISH = synth.Geometry(dim=5120, hc_mult=4, n_heads=8, max_ngram_size=4, head_
 def tiny():
     from tests.gpu_fixtures import DeviceModel
     return DeviceModel(synth.make_model(synth.TINY, synth.BASE_SEED))
+
+
+# dim 224 is not a multiple of the 256-column key tile: the forward takes the unfused path
+ODD = synth.Geometry(dim=224, hc_mult=4, n_heads=8, max_ngram_size=4, head_dim=32, vocab=1000,
+                     n_compressed=512, prime_floor=1009)
+
+
+@pytest.fixture(scope="module")
+def odd():
+    from tests.gpu_fixtures import DeviceModel
+    return DeviceModel(synth.make_model(ODD, synth.BASE_SEED + 11))
 
 
 @pytest.fixture(scope="module")
@@ -74,17 +85,23 @@ def check_against_oracle(dm, batch, r, state=None):
     assert_gate_close(r["gate"].reshape(M, -1), g2)
     value_gpu = r["kv"].reshape(M, -1)[:, g.hc_mult * g.dim:]
     assert_out_close(r["out"].reshape(M, g.hc_mult, g.dim), o2, value_gpu)
-    # 3. end to end: outliers only where a value element flipped by one ulp
-    assert_gate_close(r["gate"].reshape(M, -1), ref["gate"].reshape(M, -1))
+    # 3. end to end against the oracle's own kv. The GPU's kv may differ from the exact one
+    #    (f32 accumulation, within the projection's tolerance checked above); the part of the
+    #    gate / out difference that this causes is measured by the oracle itself, evaluated on
+    #    both kv inputs, and allowed on top of the stage tolerances.
     value_ref = ref["kv"].reshape(M, -1)[:, g.hc_mult * g.dim:]
-    bad = out_violations(r["out"].reshape(M, g.hc_mult, g.dim), ref["out"].reshape(M, g.hc_mult,
-                                                                                    g.dim), value_ref)
-    if bad.any():
-        vg, vr = bf16_to_f64(value_gpu), bf16_to_f64(value_ref)
-        tol = kv_tolerance(ref["kv"].reshape(M, -1), A, m.wkv)[:, g.hc_mult * g.dim:]
-        flipped = (vg != vr) & (np.abs(vg - vr) <= tol)
-        m_idx, s_idx, d_idx = np.nonzero(bad)
-        assert flipped[m_idx, d_idx].all(), "an output outlier is not explained by a kv flip"
+    g_ref = ref["gate"].reshape(M, -1)
+    dg_kv = np.abs(g2 - g_ref)
+    dg = np.abs(r["gate"].reshape(M, -1).astype(np.float64) - g_ref)
+    assert (dg <= GATE_ATOL + dg_kv).all(), f"gate error {dg.max():.3e} not explained by kv"
+    o = bf16_to_f64(r["out"].reshape(M, g.hc_mult, g.dim))
+    o_ref = bf16_to_f64(ref["out"].reshape(M, g.hc_mult, g.dim))
+    vr = np.abs(bf16_to_f64(value_ref))[:, None, :]
+    dv = np.abs(bf16_to_f64(value_gpu) - bf16_to_f64(value_ref))[:, None, :]
+    tol = (2 * bf16_ulp(o_ref) + (GATE_ATOL + dg_kv[:, :, None]) * vr
+           + r["gate"].reshape(M, -1)[:, :, None] * dv)
+    bad = np.abs(o - o_ref) > tol
+    assert not bad.any(), f"{bad.sum()} outputs not explained by kv; first {np.argwhere(bad)[:3]}"
     if mask is not None:
         np.testing.assert_array_equal(r["out"].reshape(M, g.hc_mult, g.dim)[~mask], x[~mask])
     return ref
@@ -94,6 +111,12 @@ def check_against_oracle(dm, batch, r, state=None):
 def test_forward_tiny(tiny, B, T):
     batch = synth.make_batch(tiny.geom, B, T, synth.BASE_SEED + 100 + T)
     check_against_oracle(tiny, batch, run_forward(tiny, batch))
+
+
+@pytest.mark.parametrize("B,T", [(1, 5), (2, 150)])
+def test_forward_unfused_geometry(odd, B, T):
+    batch = synth.make_batch(odd.geom, B, T, synth.BASE_SEED + 400 + T, mask_frac=0.2)
+    check_against_oracle(odd, batch, run_forward(odd, batch))
 
 
 @pytest.mark.parametrize("B,T,mask_frac", [(1, 1, 0.0), (2, 77, 0.0), (1, 300, 0.1),
