@@ -1,0 +1,414 @@
+#!/usr/bin/env python
+"""Benchmark of the Engram forward hot path (one layer, dim 5120, hc 4) on GB300.
+
+One step = one pass of the whole path over one batch of synthetic input: n-gram hash with the
+look-back cache (engram_hash), table-row gather + dequantisation (engram_embed_rows), and the
+fused projection + gate-and-add (engram_wkv_gate). Default workload: prefill, B=1, T=4096.
+
+Prints one JSON line (rank 0). With torchrun (N > 1) every rank runs its own batch of B
+sequences on its own GPU (sequences are independent: weak scaling, no collective on the data
+path); the step time is the max over ranks.
+
+--impl reference times the CPU oracle (oracle/) on the host cores instead, on a bounded sample of
+the same workload per step, and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "Engram tokens/s per layer (dim5120, hc4), prefill+decode; % of roofline"
+FLOPS_PER_TOKEN = 2 * 1536 * 25600           # wkv projection
+BYTES_PER_TOKEN = 40960 + 40960 + 1536 + 48  # x in, out, gathered fp8 rows, e8m0 scales
+WKV_BYTES = 25600 * 1536 * 2
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 256 << 20                   # > 129 MB L2
+
+
+def parse_args(argv=None):
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=("native", "reference"), default="native")
+    p.add_argument("--batch", type=int, default=1, help="sequences per GPU")
+    p.add_argument("--seq", type=int, default=4096, help="new tokens per sequence")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    return p.parse_args(argv)
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def shard_seed(base: int, rank: int) -> int:
+    """Each rank draws its own sequences: a disjoint shard of the global batch."""
+    return base + 1000 * rank
+
+
+def reduce_max(value: float, device=None) -> float:
+    """Max of a float over all ranks (identity without torch.distributed)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return value
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {k: float(d[k]) for k in FALLBACK_PEAKS}, "measured"
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def kernel_traffic(kernel: str):
+    """DRAM bytes per launch from the committed ncu summary, if the kernel is unchanged since."""
+    path = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)[kernel]
+        src = os.path.join(ROOT, d["source"])
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if sha != d["source_sha"]:
+            return None
+        return {"bytes_per_launch": d["bytes_per_launch"], "tokens_per_launch": d["tokens"]}
+    except (OSError, KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.3)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            f = [x.strip() for x in line.split(",")]
+            try:
+                sm.append(float(f[1]))
+                mx = max(mx, float(f[2]))
+            except (ValueError, IndexError):
+                continue
+            for name, val in zip(names, f[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------------------------- native arm
+
+
+def run_native(args):
+    import numpy as np
+    import torch
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    from deepseek_v4_engram_gb300 import build as _build
+    _build.build()
+    import deepseek_v4_engram_gb300 as eg
+    import synth
+
+    geom = synth.FULL
+    B, T = args.batch, args.seq
+    M = B * T
+    model = synth.make_model(geom, synth.BASE_SEED + 1)
+    batch = synth.make_batch(geom, B, T, shard_seed(synth.BASE_SEED + 101, rank))
+    t = model.tables
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        elif a.dtype == np.uint64:
+            a = a.view(np.int64)
+        return torch.from_numpy(a).cuda()
+
+    desc = eg.make_desc(geom.dim, geom.hc_mult, geom.n_heads, geom.max_ngram_size, geom.head_dim,
+                        t.num_embeddings, model.eps)
+    tables = eg.DeviceTables(dev(t.token_map), t.pad_id, dev(t.multipliers), dev(t.primes),
+                             dev(t.offsets))
+    weights = eg.DeviceWeights(dev(model.table), dev(model.scales), dev(model.wkv), dev(model.q),
+                               dev(model.k))
+    x = dev(batch.x)
+    tokens = dev(batch.tokens)
+    out = torch.empty_like(x)
+    steps_total = args.warmup + args.steps + 2
+    cache = torch.zeros((B, T * steps_total), dtype=torch.int32, device="cuda")
+    cache_len = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ids = torch.empty((B, T, geom.n_hash_cols), dtype=torch.int32, device="cuda")
+    rows = torch.empty((M * geom.n_hash_cols, geom.head_dim), dtype=torch.int16, device="cuda")
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.int32, device="cuda")
+    stream = torch.cuda.current_stream()
+
+    def step():
+        eg.engram_hash(desc, tables, tokens, cache, cache_len, ids)
+        eg.engram_embed_rows(desc, weights.table, weights.scales, ids.view(-1), rows)
+        k0.record(stream)
+        eg.engram_wkv_gate(desc, rows.view(M, -1), weights.wkv, x.view(M, geom.hc_mult, geom.dim),
+                           weights.q_weight, weights.k_weight, None,
+                           out.view(M, geom.hc_mult, geom.dim))
+        k1.record(stream)
+
+    k0 = torch.cuda.Event(enable_timing=True)
+    k1 = torch.cuda.Event(enable_timing=True)
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    if eg.engram_check_errors() != 0:
+        raise RuntimeError("device error word set during warm-up")
+    cache_len.zero_()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    wall0 = time.time()
+    with ClockSampler(local) as clocks:
+        for i in range(args.steps):
+            flush.zero_()                       # L2 flush between timed steps (not timed)
+            s0, kk0, kk1, s1 = ev[i]
+            s0.record(stream)
+            k0, k1 = kk0, kk1
+            step()
+            s1.record(stream)
+        torch.cuda.synchronize()
+    wall = time.time() - wall0
+    if world > 1:
+        torch.distributed.barrier()
+    step_ms = [s0.elapsed_time(s1) for s0, _, _, s1 in ev]
+    kern_ms = [a.elapsed_time(b) for _, a, b, _ in ev]
+    errors = eg.engram_check_errors()
+    total_ms = reduce_max(sum(step_ms), device="cuda")
+    value = world * M * args.steps / (total_ms / 1e3)
+
+    peaks, peak_kind = load_peaks()
+    kern_avg_s = statistics.mean(kern_ms) / 1e3
+    achieved = FLOPS_PER_TOKEN * M / kern_avg_s / 1e12
+    traffic = kernel_traffic("engram_fused_kernel")
+    roofline = {
+        "kernel": "engram_fused_kernel (projection + gate, tcgen05)",
+        "bound": "tensor", "achieved": round(achieved, 1), "peak": peaks["bf16_tflops"],
+        "unit": "TFLOP/s", "frac": round(achieved / peaks["bf16_tflops"], 4),
+        "peak_kind": f"{peak_kind} bf16 dense (burst)",
+        "frac_of_sustained": round(achieved / peaks["bf16_tflops_sustained"], 4),
+        "kernel_us": round(kern_avg_s * 1e6, 2),
+        "kernel_share_of_step": round(sum(kern_ms) / sum(step_ms), 4),
+        "traffic": (None if traffic is None else
+                    round(traffic["bytes_per_launch"] * M / traffic["tokens_per_launch"])),
+        "algorithmic_bytes": M * BYTES_PER_TOKEN + WKV_BYTES,
+    }
+    # whole-step roofline: max(FLOPs at bf16 peak, bytes at HBM peak)
+    t_roof = max(FLOPS_PER_TOKEN * M / (peaks["bf16_tflops"] * 1e12),
+                 (M * BYTES_PER_TOKEN + WKV_BYTES) / (peaks["hbm_gbs"] * 1e9))
+    step_s = total_ms / args.steps / 1e3
+
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(eg, desc, tables, weights, batch, geom, args, world)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(model, batch, budget_s=10.0)
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total_ms / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"prefill B{B} T{T} per GPU, dim 5120, hc 4, 24 rows x hd 64, "
+                               "fp8 table 12.6M rows (~805 MB), wkv 25600x1536 bf16",
+                   "global_batch": B * world, "seq_len": T, "parallelism": f"replicas x{world}",
+                   "l2": "flushed (256 MB write) between timed steps"},
+        "roofline": roofline,
+        "step_roofline_frac": round(t_roof / step_s, 4),
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary(),
+        "e2e": e2e,
+        "cpu_baseline": cpu,
+        "device_errors": errors,
+        "wall_s_timed_region": round(wall, 3),
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def run_e2e(eg, desc, tables, weights, batch, geom, args, world):
+    """Same metric through engram_forward from pinned host buffers: H2D inputs, forward, D2H out."""
+    import numpy as np
+    import torch
+    B, T = batch.tokens.shape
+    M = B * T
+    x_h = torch.from_numpy(np.ascontiguousarray(batch.x).view(np.int16)).pin_memory()
+    tok_h = torch.from_numpy(np.ascontiguousarray(batch.tokens)).pin_memory()
+    out_h = torch.empty_like(x_h).pin_memory()
+    x_d = torch.empty_like(x_h, device="cuda")
+    tok_d = torch.empty_like(tok_h, device="cuda")
+    out_d = torch.empty_like(x_d)
+    n = args.warmup + args.steps + 2
+    cache = torch.zeros((B, T * n), dtype=torch.int32, device="cuda")
+    cache_len = torch.zeros(B, dtype=torch.int32, device="cuda")
+    ws = torch.empty(eg.engram_forward_workspace_size(desc, M), dtype=torch.uint8, device="cuda")
+
+    def step():
+        x_d.copy_(x_h, non_blocking=True)
+        tok_d.copy_(tok_h, non_blocking=True)
+        eg.engram_forward(desc, tables, weights, x_d, tok_d, cache, cache_len, None, out_d, ws)
+        out_h.copy_(out_d, non_blocking=True)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    s, e = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    s.record()
+    for _ in range(args.steps):
+        step()
+    e.record()
+    torch.cuda.synchronize()
+    ms = reduce_max(s.elapsed_time(e), device="cuda")
+    return {"value": round(world * M * args.steps / (ms / 1e3), 1), "unit": "tokens/s",
+            "h2d_bytes_per_step": int(x_h.numel() * 2 + tok_h.numel() * 4),
+            "d2h_bytes_per_step": int(out_h.numel() * 2),
+            "api": "engram_forward (pinned host -> device -> host)"}
+
+
+# ---------------------------------------------------------------------------- oracle timing
+
+
+def oracle_tokens_per_s(model, batch, budget_s: float, chunk: int = 128):
+    """Run the oracle over the first tokens of sequence 0 in chunks until budget_s has passed."""
+    from oracle import engram as E
+    t = model.tables
+    g = model.geom
+    st = E.NgramHashState(t.token_map, t.pad_id, t.multipliers, t.primes, t.offsets,
+                          g.n_heads, g.max_ngram_size, 1)
+    done, t0 = 0, time.perf_counter()
+    T = batch.tokens.shape[1]
+    while done < T:
+        n = min(chunk, T - done)
+        E.forward(st, model.table, model.scales, model.wkv, model.q, model.k,
+                  batch.x[:1, done:done + n], batch.tokens[:1, done:done + n], None, model.eps)
+        done += n
+        if time.perf_counter() - t0 >= budget_s:
+            break
+    el = time.perf_counter() - t0
+    return done / el, done, el
+
+
+def host_cores() -> int:
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(model, batch, budget_s: float):
+    tps, n, el = oracle_tokens_per_s(model, batch, budget_s)
+    return {"value": round(tps, 2), "unit": "tokens/s", "cores": host_cores(), "kind": "oracle",
+            "sample": f"first {n} tokens of the same prefill workload, {el:.1f} s; float64 numpy "
+                      "(matmul through the host BLAS on all cores)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import synth
+    geom = synth.FULL
+    model = synth.make_model(geom, synth.BASE_SEED + 1)
+    batch = synth.make_batch(geom, args.batch, args.seq, synth.BASE_SEED + 101)
+    per_step = []
+    sample = 128
+    for i in range(args.warmup + args.steps):
+        tps, n, el = oracle_tokens_per_s(model, batch, budget_s=0.0, chunk=sample)
+        if i >= args.warmup:
+            per_step.append(el)
+    total = sum(per_step)
+    value = sample * args.steps / total
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(total / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "impl": "reference",
+        "config": {"workload": f"prefill B{args.batch} T{args.seq} per GPU, dim 5120, hc 4; each "
+                               f"step the oracle runs a {sample}-token sample of it",
+                   "global_batch": args.batch, "seq_len": args.seq, "parallelism": "host CPU"},
+        "cpu_baseline": {"value": round(value, 2), "unit": "tokens/s", "cores": host_cores(),
+                         "kind": "oracle", "sample": f"{sample} tokens per step"},
+        "e2e": {"value": round(value, 2), "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_native(args)
+
+
+if __name__ == "__main__":
+    main()

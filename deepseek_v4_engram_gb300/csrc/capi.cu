@@ -332,6 +332,56 @@ ENGRAM_API int engram_gate_and_add(const engram_desc_t* desc, const uint16_t* x,
   return ENGRAM_OK;
 }
 
+static FusedArgs make_fused_args(const engram_desc_t* desc, const uint16_t* rows,
+                                 const uint16_t* wkv, const uint16_t* x, const uint16_t* q,
+                                 const uint16_t* k, const uint8_t* mask, uint16_t* out,
+                                 float* gate_out, uint16_t* kv_out, int64_t M, uint32_t* err) {
+  FusedArgs f{};
+  f.a = rows;
+  f.w = wkv;
+  f.x = x;
+  f.q = q;
+  f.k = k;
+  f.mask = mask;
+  f.out = out;
+  f.gate_out = gate_out;
+  f.kv_out = kv_out;
+  f.M = M;
+  f.K = n_hash_cols(desc) * desc->head_dim;
+  f.hc = desc->hc_mult;
+  f.dim = desc->dim;
+  f.eps = desc->norm_eps;
+  f.inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));
+  f.err = err;
+  return f;
+}
+
+ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
+                               const uint16_t* wkv, const uint16_t* x, const uint16_t* q_weight,
+                               const uint16_t* k_weight, const uint8_t* token_mask, uint16_t* out,
+                               float* gate_out, uint16_t* kv_out, int64_t M, void* stream) {
+  g_msg[0] = 0;
+  int rc = gate_checks(desc, x, wkv, q_weight, k_weight, out, M);
+  if (rc || M == 0) return rc;
+  if (M >= (int64_t(1) << 31)) return fail(ENGRAM_EINVAL, "M too large");
+  const int32_t K = n_hash_cols(desc) * desc->head_dim;
+  if (!fused_supported(K, desc->hc_mult, desc->dim))
+    return fail(ENGRAM_EUNSUPPORTED,
+                "engram_wkv_gate needs n_hash_cols * head_dim %% 64 == 0, dim %% 256 == 0, "
+                "hc_mult <= 8 and dim / hc_mult a multiple of 64; use engram_wkv + "
+                "engram_gate_and_add");
+  if (!rows || !aligned(rows, 16)) return fail(ENGRAM_EINVAL, "rows must be 16-byte aligned");
+  if (kv_out && !aligned(kv_out, 16)) return fail(ENGRAM_EINVAL, "kv_out must be 16-byte aligned");
+  cudaError_t e;
+  uint32_t* err = error_word(&e);
+  if (!err) return cuda_fail(e, "engram_wkv_gate");
+  const FusedArgs f = make_fused_args(desc, rows, wkv, x, q_weight, k_weight, token_mask, out,
+                                      gate_out, kv_out, M, err);
+  if ((e = launch_fused(f, static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return cuda_fail(e, "engram_wkv_gate");
+  return ENGRAM_OK;
+}
+
 ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64_t M) {
   if (check_desc(desc) != ENGRAM_OK || M < 0) return 0;
   const size_t S = n_hash_cols(desc);
@@ -406,23 +456,8 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   const float inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));
   if (fused_supported(K, desc->hc_mult, desc->dim)) {
     // 3+4. projection with the gate fused into its epilogue
-    FusedArgs f{};
-    f.a = rows;
-    f.w = wts->wkv;
-    f.x = x;
-    f.q = wts->q_weight;
-    f.k = wts->k_weight;
-    f.mask = token_mask;
-    f.out = out;
-    f.gate_out = gate_out;
-    f.kv_out = kv_out;
-    f.M = M;
-    f.K = K;
-    f.hc = desc->hc_mult;
-    f.dim = desc->dim;
-    f.eps = desc->norm_eps;
-    f.inv_sqrt_dim = inv_sqrt_dim;
-    f.err = err;
+    const FusedArgs f = make_fused_args(desc, rows, wts->wkv, x, wts->q_weight, wts->k_weight,
+                                        token_mask, out, gate_out, kv_out, M, err);
     if ((e = launch_fused(f, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: fused");
     return ENGRAM_OK;
   }

@@ -181,6 +181,22 @@ ENGRAM_API int engram_gate_and_add(const engram_desc_t* desc, const uint16_t* x,
                                    const uint16_t* k_weight, const uint8_t* token_mask,
                                    uint16_t* out, float* gate_out, int64_t M, void* stream);
 
+/*
+ * Stages 3 + 4 in one tensor-core kernel (Engram listing, forward: self.wkv(...) followed by the
+ * gate and add): the projection of already-gathered rows with the gate-and-add in its epilogue,
+ * so the kv row is never written to memory (unless kv_out is given).
+ *   rows bf16 [M, n_hash_cols * head_dim] (the output of engram_embed_rows, flattened per token);
+ *   wkv bf16 [dim * (hc + 1), n_hash_cols * head_dim]; x, q_weight, k_weight, token_mask, out,
+ *   gate_out as in engram_gate_and_add; kv_out bf16 [M, dim * (hc + 1)] or NULL.
+ * Results equal engram_wkv followed by engram_gate_and_add up to f32 summation order in the
+ * gate. Requires n_hash_cols * head_dim % 64 == 0, dim % 256 == 0, hc_mult <= 8 and dim / hc_mult
+ * a multiple of 64; otherwise returns ENGRAM_EUNSUPPORTED (use the two separate calls).
+ */
+ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
+                               const uint16_t* wkv, const uint16_t* x, const uint16_t* q_weight,
+                               const uint16_t* k_weight, const uint8_t* token_mask, uint16_t* out,
+                               float* gate_out, uint16_t* kv_out, int64_t M, void* stream);
+
 /* Bytes of scratch engram_forward needs for M = B * T tokens (a multiple of 256). */
 ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64_t M);
 
@@ -193,9 +209,9 @@ ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64
  *   kv_out bf16 [B, T, dim * (hc + 1)] or NULL (the projection, for inspection; costs traffic);
  *   workspace: device scratch of at least engram_forward_workspace_size(desc, B * T) bytes,
  *   256-byte aligned, not shared with a concurrent call.
- * The projection and the gate run in one tensor-core kernel when the geometry allows it (K % 64
- * == 0, dim % 256 == 0, hc_mult <= 8, dim / hc_mult a multiple of 16); otherwise as separate
- * kernels. Either way every step runs on the GPU.
+ * The projection and the gate run in one tensor-core kernel (as engram_wkv_gate) when the
+ * geometry allows it; otherwise as engram_wkv then engram_gate_and_add. Either way every step
+ * runs on the GPU.
  */
 ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* tables,
                               const engram_weights_t* weights, const uint16_t* x,
