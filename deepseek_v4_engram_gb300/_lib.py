@@ -60,7 +60,11 @@ SIGNATURES = {
     "engram_forward_workspace_size": (_SZ, [_DESC, _I64]),
     "engram_forward": (ctypes.c_int, [_DESC, _TAB, _WTS, _P, _P, _I32, _I32, _P, _P, _I32, _P,
                                       _P, _P, _P, _P, _P, _SZ, _P]),
+    "engram_forward_noalloc": (ctypes.c_int, [_DESC, _TAB, _WTS, _P, _P, _I32, _I32, _P, _P,
+                                              _I32, _P, _P, _P, _P, _P, _P]),
 }
+
+NOALLOC_SCRATCH_BYTES = 8 * 1024 * 1024
 
 _lib = None
 

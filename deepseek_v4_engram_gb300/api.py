@@ -162,3 +162,17 @@ def engram_forward(desc, tables: DeviceTables, weights: DeviceWeights, x, tokens
         _ptr(hash_ids_out, "i32", "hash_ids_out"), _ptr(gate_out, "f32", "gate_out"),
         _ptr(kv_out, "bf16", "kv_out"), _ptr(workspace, "u8", "workspace"), workspace.numel(),
         _stream(stream)))
+
+
+def engram_forward_noalloc(desc, tables: DeviceTables, weights: DeviceWeights, x, tokens, cache,
+                           cache_len, token_mask, out, hash_ids_out=None, gate_out=None,
+                           kv_out=None, stream=None):
+    """engram_forward with the library's own fixed scratch instead of a workspace argument."""
+    B, T = tokens.shape
+    _check(lib().engram_forward_noalloc(
+        ctypes.byref(desc), ctypes.byref(tables.c), ctypes.byref(weights.c), _ptr(x, "bf16", "x"),
+        _ptr(tokens, "i32", "tokens"), B, T, _ptr(cache, "i32", "cache"),
+        _ptr(cache_len, "i32", "cache_len"), cache.shape[1],
+        _ptr(token_mask, "u8", "token_mask"), _ptr(out, "bf16", "out"),
+        _ptr(hash_ids_out, "i32", "hash_ids_out"), _ptr(gate_out, "f32", "gate_out"),
+        _ptr(kv_out, "bf16", "kv_out"), _stream(stream)))

@@ -191,6 +191,9 @@ bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_
   return r == CUDA_SUCCESS;
 }
 
+// Record a failure message for engram_last_error() from another translation unit.
+int set_last_error(int code, const char* msg) { return fail(code, "%s", msg); }
+
 }  // namespace engram
 
 using namespace engram;

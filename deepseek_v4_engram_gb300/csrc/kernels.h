@@ -87,6 +87,9 @@ cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t s);
 bool fused_supported(int32_t K, int32_t hc, int32_t dim);
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s);
 
+// Sets the message engram_last_error() returns on this thread; returns `code`.
+int set_last_error(int code, const char* msg);
+
 // Tensor maps (capi.cu; cuTensorMapEncodeTiled is fetched from the driver on first use).
 bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_t rows,
                         uint32_t box_inner, uint32_t box_rows);

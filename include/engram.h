@@ -221,6 +221,35 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
                               uint16_t* kv_out, void* workspace, size_t workspace_bytes,
                               void* stream);
 
+/*
+ * engram_forward without a workspace argument, for callers that cannot allocate device memory
+ * (a runtime that owns all device memory and passes a plugin only its inputs and outputs, or a
+ * serving loop that must not call cudaMalloc, which can synchronise the device). The pages have
+ * no counterpart of this call; it exists for the callers just named.
+ *
+ * Arguments and results are those of engram_forward. The scratch (hash ids and gathered rows)
+ * lives in a fixed array of ENGRAM_NOALLOC_SCRATCH_BYTES (8 MiB) that the library keeps in every
+ * GPU that loads it, until the process exits. A call whose scratch would not fit returns
+ * ENGRAM_EINVAL and launches nothing: at the full geometry (dim 5120, hc 4, 24 rows of
+ * head_dim 64) that is more than 2,647 tokens (B * T) per call; geometries that take the unfused
+ * path also keep the kv row there and fit far fewer tokens.
+ *
+ * This call allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. Its
+ * first call on a device looks up the array's device address (cudaGetSymbolAddress, with that
+ * device current); make that first call before any stream capture. Every call shares the one
+ * array and leaves its contents behind; nothing in it needs to start at zero, since each call
+ * writes all of the scratch it reads. Calls whose work overlaps on the GPU (different streams,
+ * or host threads) race on the array: serialise them.
+ */
+#define ENGRAM_NOALLOC_SCRATCH_BYTES (8 * 1024 * 1024)
+ENGRAM_API int engram_forward_noalloc(const engram_desc_t* desc, const engram_tables_t* tables,
+                                      const engram_weights_t* weights, const uint16_t* x,
+                                      const int32_t* tokens, int32_t B, int32_t T, int32_t* cache,
+                                      int32_t* cache_len, int32_t capacity,
+                                      const uint8_t* token_mask, uint16_t* out,
+                                      int32_t* hash_ids_out, float* gate_out, uint16_t* kv_out,
+                                      void* stream);
+
 #ifdef __cplusplus
 }
 #endif
