@@ -8,7 +8,7 @@
 
 #include <cudaTypedefs.h>
 
-#include "../../include/engram.h"
+#include "engram.h"
 #include "kernels.h"
 
 namespace engram {

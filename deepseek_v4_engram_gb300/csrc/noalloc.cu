@@ -8,7 +8,7 @@
 #include <cstdio>
 #include <mutex>
 
-#include "../../include/engram.h"
+#include "engram.h"
 #include "kernels.h"
 
 namespace engram {
