@@ -143,6 +143,42 @@ HashArgs make_hash_args(const engram_desc_t* d, const engram_tables_t* t, const 
 
 constexpr size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
+// How engram_forward runs stages 3 and 4 for a given token count, fastest first:
+//  - kSmall:   M <= 256: weight-streaming projection over every SM (split-K partials in f32 when
+//              the workspace holds them, else bf16 kv), then the gate kernel;
+//  - kUnfused: the persistent projection GEMM into a bf16 kv, then the gate kernel; measured
+//              faster than the fused kernel below 4096 tokens, where the fused kernel's one
+//              cluster per 128 tokens leaves most SMs idle;
+//  - kFused:   projection + gate in one kernel; kv never touches HBM; least workspace.
+enum class Path { kSmall, kUnfused, kFused };
+struct Plan {
+  Path path;
+  int ksplit;
+  size_t bytes;
+};
+constexpr int64_t kFusedMinTokens = 4096;
+
+// Candidate plans in order of preference; returns how many were written.
+int forward_plans(const engram_desc_t* d, int64_t M, Plan* out) {
+  const size_t S = n_hash_cols(d);
+  const int32_t K = static_cast<int32_t>(S) * d->head_dim;
+  const int32_t N = d->dim * (d->hc_mult + 1);
+  const size_t base = round256(size_t(M) * S * 4) + round256(size_t(M) * K * 2);
+  const size_t kv_bytes = round256(size_t(M) * N * 2);
+  const bool fused = fused_supported(K, d->hc_mult, d->dim);
+  int n = 0;
+  if (small_supported(M, N, K)) {
+    // split-K only while its f32 partial sums stay small (decode-sized batches)
+    const int ks = M <= 64 ? small_ksplit(N, K) : 1;
+    if (ks > 1) out[n++] = {Path::kSmall, ks, base + round256(size_t(ks) * M * N * 4)};
+    out[n++] = {Path::kSmall, 1, base + kv_bytes};
+  }
+  if (!fused || M < kFusedMinTokens) out[n++] = {Path::kUnfused, 1, base + kv_bytes};
+  if (fused) out[n++] = {Path::kFused, 1, base};
+  if (fused && M >= kFusedMinTokens) out[n++] = {Path::kUnfused, 1, base + kv_bytes};
+  return n;
+}
+
 }  // namespace
 
 namespace {
@@ -189,6 +225,17 @@ bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_
                               CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Smallest workspace engram_forward accepts for M tokens (0 for an invalid descriptor).
+size_t forward_min_workspace_bytes(const engram_desc_t* desc, int64_t M) {
+  if (check_desc(desc) != ENGRAM_OK || M < 0) return 0;
+  Plan plans[5];
+  const int n = forward_plans(desc, M, plans);
+  size_t best = 0;
+  for (int i = 0; i < n; ++i)
+    if (i == 0 || plans[i].bytes < best) best = plans[i].bytes;
+  return best;
 }
 
 // Record a failure message for engram_last_error() from another translation unit.
@@ -289,6 +336,20 @@ ENGRAM_API int engram_wkv(const uint16_t* a, const uint16_t* w, uint16_t* kv, in
   cudaError_t e;
   uint32_t* err = error_word(&e);
   if (!err) return cuda_fail(e, "engram_wkv");
+  if (small_supported(M, N, K)) {   // few tokens: stream the weight over every SM
+    WkvSmallArgs g{};
+    g.a = a;
+    g.w = w;
+    g.kv = kv;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.ksplit = 1;
+    g.err = err;
+    if ((e = launch_wkv_small(g, static_cast<cudaStream_t>(stream))) != cudaSuccess)
+      return cuda_fail(e, "engram_wkv");
+    return ENGRAM_OK;
+  }
   WkvArgs g{a, w, kv, M, N, K, err};
   if ((e = launch_wkv(g, static_cast<cudaStream_t>(stream))) != cudaSuccess)
     return cuda_fail(e, "engram_wkv");
@@ -387,13 +448,9 @@ ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
 
 ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64_t M) {
   if (check_desc(desc) != ENGRAM_OK || M < 0) return 0;
-  const size_t S = n_hash_cols(desc);
-  const size_t K = S * desc->head_dim;
-  const size_t N = size_t(desc->dim) * (desc->hc_mult + 1);
-  size_t bytes = round256(size_t(M) * S * 4) + round256(size_t(M) * K * 2);
-  if (!fused_supported(static_cast<int32_t>(K), desc->hc_mult, desc->dim))
-    bytes += round256(size_t(M) * N * 2);
-  return bytes;
+  Plan plans[5];
+  const int n = forward_plans(desc, M, plans);
+  return n > 0 ? plans[0].bytes : 0;
 }
 
 ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* tables,
@@ -421,9 +478,19 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   if (K % 64 != 0 || N % 32 != 0)
     return fail(ENGRAM_EUNSUPPORTED, "needs n_hash_cols * head_dim %% 64 == 0");
   if (kv_out && !aligned(kv_out, 16)) return fail(ENGRAM_EINVAL, "kv_out must be 16-byte aligned");
-  const size_t need = engram_forward_workspace_size(desc, M);
-  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
-    return fail(ENGRAM_EINVAL, "workspace must be >= %zu bytes and 256-byte aligned", need);
+  // the fastest plan whose scratch fits the workspace
+  Plan plans[5];
+  const int nplans = forward_plans(desc, M, plans);
+  const Plan* plan = nullptr;
+  size_t min_bytes = ~size_t(0);
+  for (int i = 0; i < nplans; ++i) {
+    if (plans[i].bytes < min_bytes) min_bytes = plans[i].bytes;
+    if (plan == nullptr && plans[i].bytes <= workspace_bytes) plan = &plans[i];
+  }
+  if (workspace == nullptr || plan == nullptr || !aligned(workspace, 256))
+    return fail(ENGRAM_EINVAL,
+                "workspace must be 256-byte aligned and >= %zu bytes (%zu for the fastest path)",
+                min_bytes, nplans > 0 ? plans[0].bytes : size_t(0));
 
   cudaError_t e;
   uint32_t* err = error_word(&e);
@@ -457,20 +524,41 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   if ((e = launch_rows(r, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: rows");
 
   const float inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));
-  if (fused_supported(K, desc->hc_mult, desc->dim)) {
+  if (plan->path == Path::kFused) {
     // 3+4. projection with the gate fused into its epilogue
     const FusedArgs f = make_fused_args(desc, rows, wts->wkv, x, wts->q_weight, wts->k_weight,
                                         token_mask, out, gate_out, kv_out, M, err);
     if ((e = launch_fused(f, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: fused");
     return ENGRAM_OK;
   }
-  // 3. projection -> kv [M, N]; 4. gate and add
-  uint16_t* kv = kv_out ? kv_out : reinterpret_cast<uint16_t*>(ws);
-  WkvArgs g{rows, wts->wkv, kv, M, N, K, err};
-  if ((e = launch_wkv(g, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: wkv");
+  // 3. projection -> bf16 kv (or f32 split-K partials); 4. gate and add
   GateArgs ga{};
+  if (plan->path == Path::kSmall) {
+    WkvSmallArgs g{};
+    g.a = rows;
+    g.w = wts->wkv;
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.ksplit = plan->ksplit;
+    g.err = err;
+    if (plan->ksplit > 1) {
+      g.part = reinterpret_cast<float*>(ws);
+      ga.part = g.part;
+      ga.ksplit = plan->ksplit;
+      ga.kv_out = kv_out;
+    } else {
+      g.kv = kv_out ? kv_out : reinterpret_cast<uint16_t*>(ws);
+      ga.kv = g.kv;
+    }
+    if ((e = launch_wkv_small(g, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: wkv");
+  } else {
+    uint16_t* kv = kv_out ? kv_out : reinterpret_cast<uint16_t*>(ws);
+    WkvArgs g{rows, wts->wkv, kv, M, N, K, err};
+    if ((e = launch_wkv(g, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: wkv");
+    ga.kv = kv;
+  }
   ga.x = x;
-  ga.kv = kv;
   ga.q = wts->q_weight;
   ga.k = wts->k_weight;
   ga.mask = token_mask;

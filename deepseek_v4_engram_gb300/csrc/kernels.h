@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "engram.h"
+
 namespace engram {
 
 struct HashArgs {
@@ -41,7 +43,10 @@ struct RowsArgs {
 
 struct GateArgs {
   const uint16_t* x;    // [M, hc, dim]
-  const uint16_t* kv;   // [M, dim*(hc+1)]
+  const uint16_t* kv;   // [M, dim*(hc+1)] bf16, or null when `part` is given
+  const float* part;    // [ksplit, M, dim*(hc+1)] f32 partial sums of kv, or null
+  int32_t ksplit;
+  uint16_t* kv_out;     // [M, dim*(hc+1)] or null: kv as used (bf16)
   const uint16_t* q;    // [hc, dim]
   const uint16_t* k;    // [hc, dim]
   const uint8_t* mask;  // [M] or null
@@ -59,6 +64,16 @@ struct WkvArgs {
   uint16_t* kv;       // [M, N]
   int64_t M;
   int32_t N, K;
+  uint32_t* err;
+};
+
+struct WkvSmallArgs {
+  const uint16_t* a;  // [M, K] (M <= 256)
+  const uint16_t* w;  // [N, K]
+  uint16_t* kv;       // [M, N] bf16 when ksplit == 1
+  float* part;        // [ksplit, M, N] f32 when ksplit > 1
+  int64_t M;
+  int32_t N, K, ksplit;
   uint32_t* err;
 };
 
@@ -84,8 +99,14 @@ cudaError_t launch_advance_len(int32_t* cache_len, int32_t B, int32_t T, int32_t
 cudaError_t launch_rows(const RowsArgs& a, cudaStream_t s);
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t s);
 cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t s);
+bool small_supported(int64_t M, int32_t N, int32_t K);
+int small_ksplit(int32_t N, int32_t K);
+cudaError_t launch_wkv_small(const WkvSmallArgs& a, cudaStream_t s);
 bool fused_supported(int32_t K, int32_t hc, int32_t dim);
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s);
+
+// Smallest workspace engram_forward accepts for M tokens (the fused path's, where it applies).
+size_t forward_min_workspace_bytes(const engram_desc_t* desc, int64_t M);
 
 // Sets the message engram_last_error() returns on this thread; returns `code`.
 int set_last_error(int code, const char* msg);

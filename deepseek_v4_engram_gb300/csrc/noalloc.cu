@@ -58,7 +58,8 @@ extern "C" ENGRAM_API int engram_forward_noalloc(
     int32_t* hash_ids_out, float* gate_out, uint16_t* kv_out, void* stream) {
   if (B < 0 || T < 0) return set_last_error(ENGRAM_EINVAL, "B and T must be >= 0");
   const int64_t M = int64_t(B) * T;
-  const size_t need = engram_forward_workspace_size(desc, M);
+  // engram_forward runs the fastest path whose scratch fits; the smallest one must fit here
+  const size_t need = forward_min_workspace_bytes(desc, M);
   if (need == 0 && M > 0) return set_last_error(ENGRAM_EINVAL, "invalid engram_desc_t");
   if (need > size_t(ENGRAM_NOALLOC_SCRATCH_BYTES)) {
     char msg[256];

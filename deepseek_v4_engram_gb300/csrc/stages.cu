@@ -160,13 +160,33 @@ cudaError_t launch_rows(const RowsArgs& a, cudaStream_t st) {
 
 constexpr int kGateThreads = 256;
 
+// 8 consecutive kv values (one 16-byte bf16 word) at column n of token m: either read from the
+// bf16 kv, or the f32 partial sums of the split-K projection added in K order and rounded once.
+__device__ __forceinline__ uint4 load_kv8(const GateArgs& a, int64_t m, int64_t N, int64_t n) {
+  if (a.part == nullptr) return __ldg(reinterpret_cast<const uint4*>(a.kv + m * N + n));
+  float v[8];
+  const float4* p0 = reinterpret_cast<const float4*>(a.part + m * N + n);
+  float4 lo = __ldg(p0), hi = __ldg(p0 + 1);
+  v[0] = lo.x; v[1] = lo.y; v[2] = lo.z; v[3] = lo.w;
+  v[4] = hi.x; v[5] = hi.y; v[6] = hi.z; v[7] = hi.w;
+  for (int k = 1; k < a.ksplit; ++k) {
+    const float4* pk = reinterpret_cast<const float4*>(a.part + (k * a.M + m) * N + n);
+    lo = __ldg(pk);
+    hi = __ldg(pk + 1);
+    v[0] += lo.x; v[1] += lo.y; v[2] += lo.z; v[3] += lo.w;
+    v[4] += hi.x; v[5] += hi.y; v[6] += hi.z; v[7] += hi.w;
+  }
+  return make_uint4(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]), pack_bf16x2(v[4], v[5]),
+                    pack_bf16x2(v[6], v[7]));
+}
+
 __global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
   const int64_t m = blockIdx.x / a.hc;
   const int32_t s = blockIdx.x % a.hc;
   const int64_t N = static_cast<int64_t>(a.dim) * (a.hc + 1);
   const uint16_t* xr = a.x + (m * a.hc + s) * a.dim;
-  const uint16_t* key = a.kv + m * N + static_cast<int64_t>(s) * a.dim;
-  const uint16_t* val = a.kv + m * N + static_cast<int64_t>(a.hc) * a.dim;
+  const int64_t key0 = static_cast<int64_t>(s) * a.dim;      // first key column of stream s
+  const int64_t val0 = static_cast<int64_t>(a.hc) * a.dim;   // first value column
   const uint16_t* qr = a.q + static_cast<int64_t>(s) * a.dim;
   const uint16_t* kr = a.k + static_cast<int64_t>(s) * a.dim;
   const int nvec = a.dim / 8;
@@ -174,7 +194,8 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
   float sh2 = 0.f, sk2 = 0.f, shwk = 0.f;
   for (int v = threadIdx.x; v < nvec; v += kGateThreads) {
     const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr) + v);
-    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(key) + v);
+    const uint4 kv = load_kv8(a, m, N, key0 + 8 * v);
+    if (a.kv_out) reinterpret_cast<uint4*>(a.kv_out + m * N + key0)[v] = kv;
     const uint4 qv = __ldg(reinterpret_cast<const uint4*>(qr) + v);
     const uint4 wv = __ldg(reinterpret_cast<const uint4*>(kr) + v);
     const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ks[4] = {kv.x, kv.y, kv.z, kv.w};
@@ -226,11 +247,17 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
   uint16_t* orow = a.out + (m * a.hc + s) * a.dim;
   for (int v = threadIdx.x; v < nvec; v += kGateThreads) {
     const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr) + v);
-    if (!keep) {
+    const bool write_value = a.kv_out != nullptr && s == 0;
+    if (!keep && !write_value) {
       reinterpret_cast<uint4*>(orow)[v] = xv;
       continue;
     }
-    const uint4 vv = __ldg(reinterpret_cast<const uint4*>(val) + v);
+    const uint4 vv = load_kv8(a, m, N, val0 + 8 * v);
+    if (write_value) reinterpret_cast<uint4*>(a.kv_out + m * N + val0)[v] = vv;
+    if (!keep) {
+      reinterpret_cast<uint4*>(orow)[v] = xv;   // a masked token's x passes through unchanged
+      continue;
+    }
     const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, vs[4] = {vv.x, vv.y, vv.z, vv.w};
     uint32_t o[4];
 #pragma unroll

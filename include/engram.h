@@ -197,7 +197,12 @@ ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
                                const uint16_t* k_weight, const uint8_t* token_mask, uint16_t* out,
                                float* gate_out, uint16_t* kv_out, int64_t M, void* stream);
 
-/* Bytes of scratch engram_forward needs for M = B * T tokens (a multiple of 256). */
+/*
+ * Bytes of scratch for engram_forward on M = B * T tokens with the fastest projection path (a
+ * multiple of 256). engram_forward also accepts a smaller workspace and then runs the fastest
+ * path that fits it; the smallest it accepts holds the hash ids and gathered rows (3,168 bytes
+ * per token at the full geometry, rounded up to 256 twice).
+ */
 ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64_t M);
 
 /*
@@ -207,11 +212,14 @@ ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64
  *   x bf16 [B, T, hc, dim]; token_mask uint8 [B, T] or NULL; out bf16 [B, T, hc, dim];
  *   hash_ids_out int32 [B, T, n_hash_cols] or NULL; gate_out f32 [B, T, hc] or NULL;
  *   kv_out bf16 [B, T, dim * (hc + 1)] or NULL (the projection, for inspection; costs traffic);
- *   workspace: device scratch of at least engram_forward_workspace_size(desc, B * T) bytes,
- *   256-byte aligned, not shared with a concurrent call.
- * The projection and the gate run in one tensor-core kernel (as engram_wkv_gate) when the
- * geometry allows it; otherwise as engram_wkv then engram_gate_and_add. Either way every step
- * runs on the GPU.
+ *   workspace: device scratch, 256-byte aligned, not shared with a concurrent call; see
+ *   engram_forward_workspace_size for its size.
+ * How stages 3 and 4 run depends on M and on the workspace given (the fastest path that fits):
+ * up to 256 tokens, a weight-streaming projection over every SM (split-K partials for decode-
+ * sized batches) then the gate kernel; below 4096 tokens, the persistent projection GEMM into
+ * a bf16 kv then the gate kernel; from 4096 tokens, or when only the minimum workspace is given,
+ * the projection with the gate fused into its epilogue (as engram_wkv_gate). Every path runs
+ * on the GPU; results agree within the projection's f32-summation bound.
  */
 ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* tables,
                               const engram_weights_t* weights, const uint16_t* x,

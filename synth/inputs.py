@@ -147,15 +147,28 @@ def make_scales(num_rows: int, head_dim: int, rng: np.random.Generator | None,
     raise ValueError(mode)
 
 
-def make_x(shape, rng: np.random.Generator, dist: str = "normal") -> np.ndarray:
-    """bf16 residual streams x[..., hc, dim]: N(0,1), or Student-t(nu=3)/sqrt(3) (unit rms)."""
-    if dist == "normal":
-        v = rng.standard_normal(shape, dtype=np.float32)
-    elif dist == "student_t3":
-        v = (rng.standard_t(3, size=shape) / math.sqrt(3.0)).astype(np.float32)
-    else:
-        raise ValueError(dist)
-    return _no_zeros_bf16(f32_to_bf16_bits(v))
+def make_x(shape, rng: np.random.Generator, dist: str = "normal",
+           chunk_elems: int = 1 << 24) -> np.ndarray:
+    """bf16 residual streams x[..., hc, dim]: N(0,1), or Student-t(nu=3)/sqrt(3) (unit rms).
+
+    Drawn in chunks of whole rows along the flattened leading axes, so large batches do not need
+    float64 temporaries of their full size.
+    """
+    shape = tuple(shape)
+    row = int(np.prod(shape[-2:]))
+    rows = int(np.prod(shape[:-2])) if len(shape) > 2 else 1
+    out = np.empty((rows, row), dtype=np.uint16)
+    step = max(1, chunk_elems // row)
+    for r0 in range(0, rows, step):
+        n = min(step, rows - r0)
+        if dist == "normal":
+            v = rng.standard_normal((n, row), dtype=np.float32)
+        elif dist == "student_t3":
+            v = (rng.standard_t(3, size=(n, row)) / math.sqrt(3.0)).astype(np.float32)
+        else:
+            raise ValueError(dist)
+        out[r0:r0 + n] = _no_zeros_bf16(f32_to_bf16_bits(v))
+    return out.reshape(shape)
 
 
 def make_wkv(geom: Geometry, rng: np.random.Generator) -> np.ndarray:

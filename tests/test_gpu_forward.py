@@ -47,7 +47,18 @@ def wide():
     return DeviceModel(synth.make_model(FULLISH, synth.BASE_SEED + 9, scale_mode="pow2"))
 
 
-def run_forward(dm, batch, cache=None, length=None, capacity=None):
+def ws_for(dm, M, mode):
+    """Workspace sized to select a path: "fastest" (the reported size), "kv" (room for a bf16 kv,
+    no split-K partials), or "min" (hash ids + rows only: the fused kernel)."""
+    g = dm.geom
+    r = lambda n: (n + 255) // 256 * 256
+    base = r(M * g.n_hash_cols * 4) + r(M * g.K * 2)
+    n = {"fastest": eg.engram_forward_workspace_size(dm.desc, M), "kv": base + r(M * g.N * 2),
+         "min": base}[mode]
+    return torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
+
+
+def run_forward(dm, batch, cache=None, length=None, capacity=None, ws_mode="fastest"):
     B, T = batch.tokens.shape
     g = dm.geom
     if cache is None:
@@ -56,7 +67,7 @@ def run_forward(dm, batch, cache=None, length=None, capacity=None):
     ids = torch.full((B, T, g.n_hash_cols), -1, dtype=torch.int32, device="cuda")
     gate = torch.full((B, T, g.hc_mult), float("nan"), device="cuda")
     kv = empty_bf16(B, T, g.N)
-    ws = dm.workspace(B * T)
+    ws = ws_for(dm, B * T, ws_mode)
     mask = None if batch.mask is None else dev(batch.mask)
     eg.engram_forward(dm.desc, dm.tables, dm.weights, dev(batch.x), dev(batch.tokens), cache,
                       length, mask, out, ws, hash_ids_out=ids, gate_out=gate, kv_out=kv)
@@ -107,10 +118,11 @@ def check_against_oracle(dm, batch, r, state=None):
     return ref
 
 
+@pytest.mark.parametrize("ws_mode", ["fastest", "kv", "min"])
 @pytest.mark.parametrize("B,T", [(1, 16), (2, 17), (1, 129), (3, 100)])
-def test_forward_tiny(tiny, B, T):
+def test_forward_tiny(tiny, B, T, ws_mode):
     batch = synth.make_batch(tiny.geom, B, T, synth.BASE_SEED + 100 + T)
-    check_against_oracle(tiny, batch, run_forward(tiny, batch))
+    check_against_oracle(tiny, batch, run_forward(tiny, batch, ws_mode=ws_mode))
 
 
 @pytest.mark.parametrize("B,T", [(1, 5), (2, 150)])
@@ -119,12 +131,13 @@ def test_forward_unfused_geometry(odd, B, T):
     check_against_oracle(odd, batch, run_forward(odd, batch))
 
 
+@pytest.mark.parametrize("ws_mode", ["fastest", "kv", "min"])
 @pytest.mark.parametrize("B,T,mask_frac", [(1, 1, 0.0), (2, 77, 0.0), (1, 300, 0.1),
-                                           (4, 160, 0.1)])
-def test_forward_full_width(wide, B, T, mask_frac):
+                                           (4, 160, 0.1), (64, 1, 0.0)])
+def test_forward_full_width(wide, B, T, mask_frac, ws_mode):
     batch = synth.make_batch(wide.geom, B, T, synth.BASE_SEED + 200 + T, x_dist="student_t3",
                              mask_frac=mask_frac)
-    check_against_oracle(wide, batch, run_forward(wide, batch))
+    check_against_oracle(wide, batch, run_forward(wide, batch, ws_mode=ws_mode))
 
 
 def test_prefill_then_decode_equals_one_prefill(wide):
@@ -138,6 +151,10 @@ def test_prefill_then_decode_equals_one_prefill(wide):
     for t in range(T - j, T):
         step = synth.Batch(batch.tokens[:, t:t + 1], batch.x[:, t:t + 1], None)
         parts.append(run_forward(wide, step, cache, length))
-    for key in ("hash_ids", "out", "kv"):
-        np.testing.assert_array_equal(np.concatenate([p[key] for p in parts], 1), whole[key])
+    # the hash is integer-exact across the split; out and kv of the split run come from other
+    # projection kernels (token counts pick the path), so they are checked against the oracle
+    np.testing.assert_array_equal(np.concatenate([p["hash_ids"] for p in parts], 1),
+                                  whole["hash_ids"])
     np.testing.assert_array_equal(host(length), [T] * B)
+    split = {k: np.concatenate([p[k] for p in parts], 1) for k in ("hash_ids", "out", "kv", "gate")}
+    check_against_oracle(wide, batch, split)

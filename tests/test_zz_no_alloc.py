@@ -42,9 +42,11 @@ def run(dm, batch, noalloc: bool):
                                       dev(batch.tokens), cache, length, mask, out,
                                       hash_ids_out=ids, gate_out=gate)
     else:
+        # the caller-workspace entry point, given a workspace as large as the library's own
+        # scratch, so that both calls choose the same projection path
+        ws = torch.empty(_lib.NOALLOC_SCRATCH_BYTES, dtype=torch.uint8, device="cuda")
         eg.engram_forward(dm.desc, dm.tables, dm.weights, dev(batch.x), dev(batch.tokens), cache,
-                          length, mask, out, dm.workspace(B * T), hash_ids_out=ids, gate_out=gate,
-                          kv_out=kv)
+                          length, mask, out, ws, hash_ids_out=ids, gate_out=gate, kv_out=kv)
     assert eg.engram_check_errors() == 0
     return host(out), host(ids), host(gate), host(length), None if kv is None else host(kv)
 
