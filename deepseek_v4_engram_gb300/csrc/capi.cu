@@ -70,8 +70,8 @@ int check_desc(const engram_desc_t* d) {
   if (d == nullptr) return fail(ENGRAM_EINVAL, "desc is NULL");
   if (d->dim <= 0 || d->hc_mult <= 0 || d->n_heads <= 0 || d->head_dim <= 0)
     return fail(ENGRAM_EINVAL, "dim, hc_mult, n_heads and head_dim must be > 0");
-  if (d->max_ngram_size < 2 || d->max_ngram_size > 64)
-    return fail(ENGRAM_EINVAL, "max_ngram_size must be in [2, 64]");
+  if (d->max_ngram_size < 2 || d->max_ngram_size > 8)
+    return fail(ENGRAM_EINVAL, "max_ngram_size must be in [2, 8]");
   if (d->head_dim % 32 != 0)
     return fail(ENGRAM_EINVAL, "head_dim must be a multiple of 32 (one e8m0 scale per 32)");
   if (d->dim % 8 != 0) return fail(ENGRAM_EINVAL, "dim must be a multiple of 8");
@@ -163,7 +163,7 @@ int forward_plans(const engram_desc_t* d, int64_t M, Plan* out) {
   const size_t S = n_hash_cols(d);
   const int32_t K = static_cast<int32_t>(S) * d->head_dim;
   const int32_t N = d->dim * (d->hc_mult + 1);
-  const size_t base = round256(size_t(M) * S * 4) + round256(size_t(M) * K * 2);
+  const size_t base = round256(size_t(M) * K * 2);   // gathered rows (hash ids stay on chip)
   const size_t kv_bytes = round256(size_t(M) * N * 2);
   const bool fused = fused_supported(K, d->hc_mult, d->dim);
   int n = 0;
@@ -497,38 +497,33 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   if (!err) return cuda_fail(e, "engram_forward");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int32_t* ids = reinterpret_cast<int32_t*>(ws);
-  ws += round256(size_t(M) * S * 4);
-  if (hash_ids_out) ids = hash_ids_out;
-  uint16_t* rows = reinterpret_cast<uint16_t*>(ws);
+  uint16_t* rows = reinterpret_cast<uint16_t*>(ws);   // the projection's input [M, K]
   ws += round256(size_t(M) * K * 2);
 
-  // 1. hash (reads cache_len; the row gather below advances it once the hash has run)
-  const HashArgs h = make_hash_args(desc, tables, tokens, B, T, cache, cache_len, capacity, ids,
-                                    err);
-  if ((e = launch_hash(h, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: hash");
-  // 2. gather + dequantise rows -> A [M, K]
-  RowsArgs r{};
-  r.table = wts->table;
-  r.scales = wts->scales;
-  r.ids = ids;
-  r.n_ids = M * S;
-  r.num_rows = desc->num_embeddings;
-  r.head_dim = desc->head_dim;
-  r.out = rows;
-  r.adv_len = cache_len;
-  r.adv_B = B;
-  r.adv_T = T;
-  r.adv_cap = capacity;
-  r.err = err;
-  if ((e = launch_rows(r, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: rows");
+  // 1+2. hash every slot and gather its row into the projection's input, in one kernel. The
+  // kernels of the chain are launched with programmatic stream serialization: each overlaps its
+  // launch and prologue with the previous one and waits for it before touching its data.
+  HashArgs h = make_hash_args(desc, tables, tokens, B, T, cache, cache_len, capacity,
+                              hash_ids_out, err);
+  HashRowsArgs hr{};
+  hr.hash = h;
+  hr.table = wts->table;
+  hr.scales = wts->scales;
+  hr.num_rows = desc->num_embeddings;
+  hr.head_dim = desc->head_dim;
+  hr.rows = rows;
+  if ((e = launch_hash_rows(hr, st, true)) != cudaSuccess)
+    return cuda_fail(e, "engram_forward: hash + rows");
+  // the last kernel of the chain advances the cache lengths (every reader of them is done)
+  const LenAdvance adv{cache_len, B, T, capacity};
 
   const float inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));
   if (plan->path == Path::kFused) {
     // 3+4. projection with the gate fused into its epilogue
-    const FusedArgs f = make_fused_args(desc, rows, wts->wkv, x, wts->q_weight, wts->k_weight,
-                                        token_mask, out, gate_out, kv_out, M, err);
-    if ((e = launch_fused(f, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: fused");
+    FusedArgs f = make_fused_args(desc, rows, wts->wkv, x, wts->q_weight, wts->k_weight,
+                                  token_mask, out, gate_out, kv_out, M, err);
+    f.adv = adv;
+    if ((e = launch_fused(f, st, true)) != cudaSuccess) return cuda_fail(e, "engram_forward: fused");
     return ENGRAM_OK;
   }
   // 3. projection -> bf16 kv (or f32 split-K partials); 4. gate and add
@@ -551,11 +546,12 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
       g.kv = kv_out ? kv_out : reinterpret_cast<uint16_t*>(ws);
       ga.kv = g.kv;
     }
-    if ((e = launch_wkv_small(g, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: wkv");
+    if ((e = launch_wkv_small(g, st, true)) != cudaSuccess)
+      return cuda_fail(e, "engram_forward: wkv");
   } else {
     uint16_t* kv = kv_out ? kv_out : reinterpret_cast<uint16_t*>(ws);
     WkvArgs g{rows, wts->wkv, kv, M, N, K, err};
-    if ((e = launch_wkv(g, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: wkv");
+    if ((e = launch_wkv(g, st, true)) != cudaSuccess) return cuda_fail(e, "engram_forward: wkv");
     ga.kv = kv;
   }
   ga.x = x;
@@ -569,7 +565,8 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   ga.dim = desc->dim;
   ga.eps = desc->norm_eps;
   ga.inv_sqrt_dim = inv_sqrt_dim;
-  if ((e = launch_gate(ga, st)) != cudaSuccess) return cuda_fail(e, "engram_forward: gate");
+  ga.adv = adv;
+  if ((e = launch_gate(ga, st, true)) != cudaSuccess) return cuda_fail(e, "engram_forward: gate");
   return ENGRAM_OK;
 }
 

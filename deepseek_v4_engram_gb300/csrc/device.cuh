@@ -34,6 +34,20 @@ __device__ __forceinline__ void set_error(uint32_t* err, uint32_t bits) {
   if (err) atomicOr(err, bits);
 }
 
+// ------------------------------------------------------------- programmatic dependent launch
+// A kernel launched with programmatic stream serialization may start before the kernel ahead of
+// it in the stream has finished. pdl_wait() blocks until that kernel has completed and its
+// writes are visible (a no-op for an ordinary launch); pdl_launch_dependents() lets the next
+// kernel begin launching. Every kernel of the forward chain waits before it touches memory that
+// an earlier kernel writes, and triggers its dependents only after its own wait, so each early
+// start still sees everything that came before it.
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------------------ mbarrier
 
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -62,6 +62,7 @@ struct FusedParams {
   int32_t K, hc, dim, bnv;
   float eps, inv_sqrt_dim;
   uint32_t* err;
+  LenAdvance adv;
 };
 
 // Value columns per CTA are split into tiles of bnv columns: the largest multiple of 64 that
@@ -181,6 +182,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
   volatile int* abort = &sh->abort;
+  pdl_wait();   // rows (and the cache lengths) come from the previous kernel of the stream
+  pdl_launch_dependents();
+  if (p.adv.len != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 32)
+    for (int32_t b = threadIdx.x; b < p.adv.B; b += 32)
+      p.adv.len[b] = min(p.adv.len[b] + p.adv.T, p.adv.cap);
 
   if (warp == 0) {
     // ------------------------------------------------------------- GEMM operand producer
@@ -387,7 +393,7 @@ bool fused_supported(int32_t K, int32_t hc, int32_t dim) {
          value_tile_width(hc, dim) > 0;
 }
 
-cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st) {
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl) {
   const int bnv = value_tile_width(a.hc, a.dim);
   const int64_t N = static_cast<int64_t>(a.dim) * (a.hc + 1);
   alignas(64) CUtensorMap tmA, tmWk, tmWv, tmX;
@@ -419,19 +425,22 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st) {
   p.eps = a.eps;
   p.inv_sqrt_dim = a.inv_sqrt_dim;
   p.err = a.err;
+  p.adv = a.adv;
 
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(static_cast<unsigned>(a.hc), static_cast<unsigned>((a.M + kBM - 1) / kBM), 1);
   cfg.blockDim = dim3(kFusedThreads, 1, 1);
   cfg.dynamicSmemBytes = kFusedSmem;
   cfg.stream = st;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = static_cast<unsigned>(a.hc);
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = pdl ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, engram_fused_kernel, tmA, tmWk, tmWv, tmX, p);
 }
 

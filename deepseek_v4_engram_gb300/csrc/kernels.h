@@ -6,6 +6,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include <utility>
+
 #include "engram.h"
 
 namespace engram {
@@ -24,6 +26,23 @@ struct HashArgs {
   const int64_t* offsets;       // [S]
   int32_t n_heads, max_ngram;
   uint32_t* err;
+};
+
+// Stages 1 + 2 in one kernel: hash a position's slot and gather + dequantise its table row.
+struct HashRowsArgs {
+  HashArgs hash;          // hash.hash_ids may be null (ids then stay in registers)
+  const uint8_t* table;   // [rows, hd] e4m3
+  const uint8_t* scales;  // [rows, hd/32] e8m0
+  int64_t num_rows;
+  int32_t head_dim;
+  uint16_t* rows;         // [B*T, S, hd] bf16
+};
+
+// Advance cache_len[b] += T (clamped to capacity) for b < B; done by one block of the last kernel
+// of the forward, once every reader of the old lengths has finished.
+struct LenAdvance {
+  int32_t* len;
+  int32_t B, T, cap;
 };
 
 struct RowsArgs {
@@ -56,6 +75,7 @@ struct GateArgs {
   int32_t hc, dim;
   float eps;
   float inv_sqrt_dim;
+  LenAdvance adv;       // adv.len may be null
 };
 
 struct WkvArgs {
@@ -91,19 +111,40 @@ struct FusedArgs {
   int32_t K, hc, dim;
   float eps, inv_sqrt_dim;
   uint32_t* err;
+  LenAdvance adv;         // adv.len may be null
 };
 
+// `pdl`: launch with programmatic stream serialization (the kernel then overlaps its launch and
+// prologue with the previous kernel of the stream and waits for it before touching its data).
+cudaError_t launch_hash_rows(const HashRowsArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_hash(const HashArgs& a, cudaStream_t s);
 cudaError_t launch_advance_len(int32_t* cache_len, int32_t B, int32_t T, int32_t cap,
                                cudaStream_t s);
 cudaError_t launch_rows(const RowsArgs& a, cudaStream_t s);
-cudaError_t launch_gate(const GateArgs& a, cudaStream_t s);
-cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t s);
+cudaError_t launch_gate(const GateArgs& a, cudaStream_t s, bool pdl = false);
+cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t s, bool pdl = false);
 bool small_supported(int64_t M, int32_t N, int32_t K);
 int small_ksplit(int32_t N, int32_t K);
-cudaError_t launch_wkv_small(const WkvSmallArgs& a, cudaStream_t s);
+cudaError_t launch_wkv_small(const WkvSmallArgs& a, cudaStream_t s, bool pdl = false);
 bool fused_supported(int32_t K, int32_t hc, int32_t dim);
-cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s);
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s, bool pdl = false);
+
+// cudaLaunchKernelEx with optional programmatic stream serialization.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                      cudaStream_t st, bool pdl, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Smallest workspace engram_forward accepts for M tokens (the fused path's, where it applies).
 size_t forward_min_workspace_bytes(const engram_desc_t* desc, int64_t M);

@@ -87,17 +87,34 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
 
   if (warp == 0) {
     if (lane == 0) {
-      // producer: a ring of S stages (the ring helper is sized for the maximum depth)
+      // producer: a ring of S stages. The wkv slices do not depend on earlier kernels, so the
+      // first stages' weight loads are issued before waiting for the kernel that wrote the
+      // activations (with a programmatic launch that wait overlaps the previous kernel's tail).
       uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
+      int pre = 0;
+      if (static_cast<int>(blockIdx.x) < items) {
+        const int n0 = (blockIdx.x / p.ksplit) * kSmallBM;
+        const int kb0 = (blockIdx.x % p.ksplit) * kb_per;
+        pre = kb_per < S ? kb_per : S;
+        for (int j = 0; j < pre; ++j) {
+          mbar_arrive_expect_tx(&sh->full[j], a_bytes + b_bytes);
+          tma_load_2d(smem + j * stage_bytes, &tmW, &sh->full[j], (kb0 + j) * kBK, n0);
+        }
+      }
+      pdl_wait();
+      pdl_launch_dependents();
       bool ok = true;
+      int g = 0;   // kblocks issued by this CTA so far
       for (int it = blockIdx.x; it < items && ok && !*abort; it += gridDim.x) {
         const int n0 = (it / p.ksplit) * kSmallBM;
         const int kb0 = (it % p.ksplit) * kb_per;
-        for (int kb = kb0; kb < kb0 + kb_per; ++kb) {
-          if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort, p.err)) { ok = false; break; }
+        for (int kb = kb0; kb < kb0 + kb_per; ++kb, ++g) {
           uint8_t* st = smem + stage * stage_bytes;
-          mbar_arrive_expect_tx(&sh->full[stage], a_bytes + b_bytes);
-          tma_load_2d(st, &tmW, &sh->full[stage], kb * kBK, n0);
+          if (g >= pre) {
+            if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort, p.err)) { ok = false; break; }
+            mbar_arrive_expect_tx(&sh->full[stage], a_bytes + b_bytes);
+            tma_load_2d(st, &tmW, &sh->full[stage], kb * kBK, n0);
+          }
           tma_load_2d(st + a_bytes, &tmA, &sh->full[stage], kb * kBK, 0);
           issued_mask |= 1u << stage;
           issued_parity = (issued_parity & ~(1u << stage)) | (phase << stage);
@@ -211,7 +228,7 @@ int small_ksplit(int32_t N, int32_t K) {
   return best;
 }
 
-cudaError_t launch_wkv_small(const WkvSmallArgs& a, cudaStream_t st) {
+cudaError_t launch_wkv_small(const WkvSmallArgs& a, cudaStream_t st, bool pdl) {
   const int nt = static_cast<int>((a.M + 31) / 32 * 32);   // tokens per MMA, a multiple of 32
   alignas(64) CUtensorMap tmW, tmA;
   if (!tensor_map_2d_bf16(&tmW, a.w, a.K, a.N, kBK, kSmallBM) ||
@@ -241,8 +258,7 @@ cudaError_t launch_wkv_small(const WkvSmallArgs& a, cudaStream_t st) {
   p.err = a.err;
   const int items = (a.N / kSmallBM) * a.ksplit;
   const int grid = items < sm_count() ? items : sm_count();
-  wkv_small_kernel<<<grid, kSmallThreads, smem, st>>>(tmW, tmA, p);
-  return cudaGetLastError();
+  return launch_ex(wkv_small_kernel, dim3(grid), dim3(kSmallThreads), smem, st, pdl, tmW, tmA, p);
 }
 
 }  // namespace engram

@@ -29,11 +29,9 @@ __device__ __forceinline__ int32_t compressed_id(const HashArgs& a, int32_t b, i
   return a.cache[static_cast<int64_t>(b) * a.capacity + q];
 }
 
-__global__ void __launch_bounds__(256) hash_kernel(HashArgs a) {
+// Hash id of flat work item i = (b, t, s); appends c_p to the cache when s == 0.
+__device__ __forceinline__ int32_t hash_slot(const HashArgs& a, int64_t i) {
   const int32_t S = (a.max_ngram - 1) * a.n_heads;
-  const int64_t total = static_cast<int64_t>(a.B) * a.T * S;
-  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= total) return;
   const int32_t s = static_cast<int32_t>(i % S);
   const int64_t bt = i / S;
   const int32_t t = static_cast<int32_t>(bt % a.T);
@@ -49,7 +47,7 @@ __global__ void __launch_bounds__(256) hash_kernel(HashArgs a) {
     mix ^= static_cast<uint64_t>(static_cast<int64_t>(c)) * __ldg(a.multipliers + k);
   }
   const uint64_t P = __ldg(a.primes + s);
-  a.hash_ids[i] = static_cast<int32_t>(static_cast<int64_t>(mix % P) + __ldg(a.offsets + s));
+  const int32_t id = static_cast<int32_t>(static_cast<int64_t>(mix % P) + __ldg(a.offsets + s));
 
   if (s == 0) {  // one thread per position appends c_p to the cache
     const int64_t p = static_cast<int64_t>(len0) + t;
@@ -59,6 +57,15 @@ __global__ void __launch_bounds__(256) hash_kernel(HashArgs a) {
       set_error(a.err, kErrCacheCapacity);
     }
   }
+  return id;
+}
+
+__global__ void __launch_bounds__(256) hash_kernel(HashArgs a) {
+  const int32_t S = (a.max_ngram - 1) * a.n_heads;
+  const int64_t total = static_cast<int64_t>(a.B) * a.T * S;
+  const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= total) return;
+  a.hash_ids[i] = hash_slot(a, i);
 }
 
 __global__ void advance_len_kernel(int32_t* len, int32_t B, int32_t T, int32_t cap) {
@@ -144,6 +151,100 @@ __global__ void __launch_bounds__(256) rows_kernel(RowsArgs a) {
   }
 }
 
+// Stages 1 + 2 in one kernel, so the ids never make a round trip through memory. A block takes
+// kHrPositions consecutive positions: first one thread per (position, look-back k) resolves the
+// compressed id c_{p-k} (token map, cache or pad) into shared memory and appends c_p to the
+// cache; then one thread per (position, slot) forms the slot's mix and id from shared memory and
+// gathers + dequantises its table row (independent 16-byte loads).
+constexpr int kHrPositions = 8;
+constexpr int kHrMaxNgram = 8;
+constexpr int kHrThreads = 256;
+
+__global__ void __launch_bounds__(kHrThreads) hash_rows_kernel(HashRowsArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const HashArgs& h = a.hash;
+  const int32_t S = (h.max_ngram - 1) * h.n_heads;
+  const int64_t M = static_cast<int64_t>(h.B) * h.T;
+  const int64_t pos0 = static_cast<int64_t>(blockIdx.x) * kHrPositions;
+  __shared__ int32_t cwin[kHrPositions][kHrMaxNgram];
+
+  // phase 1: the window c_{p-k} of every position of the block
+  if (threadIdx.x < kHrPositions * h.max_ngram) {
+    const int j = threadIdx.x / h.max_ngram, k = threadIdx.x % h.max_ngram;
+    const int64_t bt = pos0 + j;
+    if (bt < M) {
+      const int32_t b = static_cast<int32_t>(bt / h.T), t = static_cast<int32_t>(bt % h.T);
+      const int32_t len0 = h.cache_len[b];
+      const int32_t c = compressed_id(h, b, t, len0, k);
+      cwin[j][k] = c;
+      if (k == 0) {
+        const int64_t p = static_cast<int64_t>(len0) + t;
+        if (p < h.capacity)
+          h.cache[static_cast<int64_t>(b) * h.capacity + p] = c;
+        else
+          set_error(h.err, kErrCacheCapacity);
+      }
+    }
+  }
+  __syncthreads();
+
+  // phase 2: slot ids and rows
+  const int32_t chunks = a.head_dim / 16;
+  for (int item = threadIdx.x; item < kHrPositions * S; item += kHrThreads) {
+    const int j = item / S, s = item % S;
+    const int64_t bt = pos0 + j;
+    if (bt >= M) break;
+    const int32_t n = s / h.n_heads + 2;
+    uint64_t mix = 0;
+    for (int32_t k = 0; k < n; ++k)
+      mix ^= static_cast<uint64_t>(static_cast<int64_t>(cwin[j][k])) * __ldg(h.multipliers + k);
+    const int32_t id =
+        static_cast<int32_t>(static_cast<int64_t>(mix % __ldg(h.primes + s)) + __ldg(h.offsets + s));
+    const int64_t i = bt * S + s;
+    if (h.hash_ids) h.hash_ids[i] = id;
+    uint4* dst = reinterpret_cast<uint4*>(a.rows + i * a.head_dim);
+    if (id < 0 || id >= a.num_rows) {
+      set_error(h.err, kErrIdRange);
+      for (int32_t c = 0; c < 2 * chunks; ++c) dst[c] = make_uint4(0, 0, 0, 0);
+      continue;
+    }
+    const uint4* src =
+        reinterpret_cast<const uint4*>(a.table + static_cast<int64_t>(id) * a.head_dim);
+    const uint8_t* sc = a.scales + static_cast<int64_t>(id) * (a.head_dim / 32);
+    if (chunks == 4) {   // head_dim 64: all four loads in flight at once
+      uint4 code[4];
+      uint32_t scl[2];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) code[c] = __ldg(src + c);
+      scl[0] = __ldg(sc);
+      scl[1] = __ldg(sc + 1);
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint4 lo, hi;
+        dequant16(code[c], e8m0_to_f32(scl[c / 2]), lo, hi);
+        dst[2 * c] = lo;
+        dst[2 * c + 1] = hi;
+      }
+    } else {
+      for (int32_t c = 0; c < chunks; ++c) {
+        uint4 lo, hi;
+        dequant16(__ldg(src + c), e8m0_to_f32(__ldg(sc + c / 2)), lo, hi);
+        dst[2 * c] = lo;
+        dst[2 * c + 1] = hi;
+      }
+    }
+  }
+}
+
+cudaError_t launch_hash_rows(const HashRowsArgs& a, cudaStream_t st, bool pdl) {
+  if (a.hash.max_ngram > kHrMaxNgram) return cudaErrorInvalidValue;
+  const int64_t M = static_cast<int64_t>(a.hash.B) * a.hash.T;
+  const int64_t blocks = (M + kHrPositions - 1) / kHrPositions;
+  return launch_ex(hash_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kHrThreads), 0, st,
+                   pdl, a);
+}
+
 cudaError_t launch_rows(const RowsArgs& a, cudaStream_t st) {
   const int64_t total = a.n_ids * (a.head_dim / 16);
   int64_t blocks = (total + 255) / 256;
@@ -180,41 +281,47 @@ __device__ __forceinline__ uint4 load_kv8(const GateArgs& a, int64_t m, int64_t 
                     pack_bf16x2(v[6], v[7]));
 }
 
-__global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
-  const int64_t m = blockIdx.x / a.hc;
-  const int32_t s = blockIdx.x % a.hc;
-  const int64_t N = static_cast<int64_t>(a.dim) * (a.hc + 1);
-  const uint16_t* xr = a.x + (m * a.hc + s) * a.dim;
-  const int64_t key0 = static_cast<int64_t>(s) * a.dim;      // first key column of stream s
-  const int64_t val0 = static_cast<int64_t>(a.hc) * a.dim;   // first value column
-  const uint16_t* qr = a.q + static_cast<int64_t>(s) * a.dim;
-  const uint16_t* kr = a.k + static_cast<int64_t>(s) * a.dim;
-  const int nvec = a.dim / 8;
+__device__ __forceinline__ void advance_lengths(const LenAdvance& adv) {
+  if (adv.len != nullptr && blockIdx.x == 0)
+    for (int32_t b = threadIdx.x; b < adv.B; b += blockDim.x)
+      adv.len[b] = min(adv.len[b] + adv.T, adv.cap);
+}
 
-  float sh2 = 0.f, sk2 = 0.f, shwk = 0.f;
-  for (int v = threadIdx.x; v < nvec; v += kGateThreads) {
-    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr) + v);
-    const uint4 kv = load_kv8(a, m, N, key0 + 8 * v);
-    if (a.kv_out) reinterpret_cast<uint4*>(a.kv_out + m * N + key0)[v] = kv;
-    const uint4 qv = __ldg(reinterpret_cast<const uint4*>(qr) + v);
-    const uint4 wv = __ldg(reinterpret_cast<const uint4*>(kr) + v);
-    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ks[4] = {kv.x, kv.y, kv.z, kv.w};
-    const uint32_t qs[4] = {qv.x, qv.y, qv.z, qv.w}, ws[4] = {wv.x, wv.y, wv.z, wv.w};
+__device__ __forceinline__ void acc_sums(uint4 xv, uint4 kv, uint4 qv, uint4 wv, float& sh2,
+                                         float& sk2, float& shwk) {
+  const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, ks[4] = {kv.x, kv.y, kv.z, kv.w};
+  const uint32_t qs[4] = {qv.x, qv.y, qv.z, qv.w}, ws[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
+  for (int j = 0; j < 4; ++j) {
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        const int sh = half * 16;
-        const float h = bf16_bits_to_f32((xs[j] >> sh) & 0xFFFFu);
-        const float kk = bf16_bits_to_f32((ks[j] >> sh) & 0xFFFFu);
-        const float w = bf16_bits_to_f32((qs[j] >> sh) & 0xFFFFu) *
-                        bf16_bits_to_f32((ws[j] >> sh) & 0xFFFFu);
-        sh2 = fmaf(h, h, sh2);
-        sk2 = fmaf(kk, kk, sk2);
-        shwk = fmaf(h * w, kk, shwk);
-      }
+    for (int half = 0; half < 2; ++half) {
+      const int sh = half * 16;
+      const float h = bf16_bits_to_f32((xs[j] >> sh) & 0xFFFFu);
+      const float kk = bf16_bits_to_f32((ks[j] >> sh) & 0xFFFFu);
+      const float w = bf16_bits_to_f32((qs[j] >> sh) & 0xFFFFu) *
+                      bf16_bits_to_f32((ws[j] >> sh) & 0xFFFFu);
+      sh2 = fmaf(h, h, sh2);
+      sk2 = fmaf(kk, kk, sk2);
+      shwk = fmaf(h * w, kk, shwk);
     }
   }
+}
+
+__device__ __forceinline__ uint4 gate_out8(uint4 xv, uint4 vv, float g) {
+  const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, vs[4] = {vv.x, vv.y, vv.z, vv.w};
+  uint32_t o[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float h0 = bf16_bits_to_f32(xs[j] & 0xFFFFu), h1 = bf16_bits_to_f32(xs[j] >> 16);
+    const float v0 = bf16_bits_to_f32(vs[j] & 0xFFFFu), v1 = bf16_bits_to_f32(vs[j] >> 16);
+    o[j] = pack_bf16x2(fmaf(g, v0, h0), fmaf(g, v1, h1));
+  }
+  return make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// Block reduction of the three sums; returns the gate (0 for a masked token) to every thread.
+__device__ __forceinline__ float block_gate(const GateArgs& a, int64_t m, int32_t s, float sh2,
+                                            float sk2, float shwk) {
   __shared__ float red[3][kGateThreads / 32];
   __shared__ float gate_s;
   sh2 = warp_sum(sh2);
@@ -242,38 +349,85 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
     }
   }
   __syncthreads();
-  const float g = gate_s;
+  return gate_s;
+}
+
+// One block per (token, stream). kVec > 0: each thread keeps its (at most kVec) 8-element
+// vectors of x, key and value in registers (dim <= 8 * kVec * kGateThreads), and the value loads
+// are issued before the reduction; kVec == 0: any dim, two passes over x.
+template <int kVec>
+__global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
+  pdl_wait();
+  pdl_launch_dependents();
+  advance_lengths(a.adv);
+  const int64_t m = blockIdx.x / a.hc;
+  const int32_t s = blockIdx.x % a.hc;
+  const int64_t N = static_cast<int64_t>(a.dim) * (a.hc + 1);
+  const uint16_t* xr = a.x + (m * a.hc + s) * a.dim;
+  const int64_t key0 = static_cast<int64_t>(s) * a.dim;      // first key column of stream s
+  const int64_t val0 = static_cast<int64_t>(a.hc) * a.dim;   // first value column
+  const uint16_t* qr = a.q + static_cast<int64_t>(s) * a.dim;
+  const uint16_t* kr = a.k + static_cast<int64_t>(s) * a.dim;
+  const int nvec = a.dim / 8;
   const bool keep = a.mask == nullptr || a.mask[m] != 0;
+  const bool write_value = a.kv_out != nullptr && s == 0;
   uint16_t* orow = a.out + (m * a.hc + s) * a.dim;
-  for (int v = threadIdx.x; v < nvec; v += kGateThreads) {
-    const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr) + v);
-    const bool write_value = a.kv_out != nullptr && s == 0;
-    if (!keep && !write_value) {
-      reinterpret_cast<uint4*>(orow)[v] = xv;
-      continue;
-    }
-    const uint4 vv = load_kv8(a, m, N, val0 + 8 * v);
-    if (write_value) reinterpret_cast<uint4*>(a.kv_out + m * N + val0)[v] = vv;
-    if (!keep) {
-      reinterpret_cast<uint4*>(orow)[v] = xv;   // a masked token's x passes through unchanged
-      continue;
-    }
-    const uint32_t xs[4] = {xv.x, xv.y, xv.z, xv.w}, vs[4] = {vv.x, vv.y, vv.z, vv.w};
-    uint32_t o[4];
+  float sh2 = 0.f, sk2 = 0.f, shwk = 0.f;
+
+  if constexpr (kVec > 0) {
+    uint4 xv[kVec], vv[kVec];
 #pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float h0 = bf16_bits_to_f32(xs[j] & 0xFFFFu), h1 = bf16_bits_to_f32(xs[j] >> 16);
-      const float v0 = bf16_bits_to_f32(vs[j] & 0xFFFFu), v1 = bf16_bits_to_f32(vs[j] >> 16);
-      o[j] = pack_bf16x2(fmaf(g, v0, h0), fmaf(g, v1, h1));
+    for (int j = 0; j < kVec; ++j) {
+      const int v = threadIdx.x + j * kGateThreads;
+      if (v < nvec) {
+        xv[j] = __ldg(reinterpret_cast<const uint4*>(xr) + v);
+        const uint4 kv = load_kv8(a, m, N, key0 + 8 * v);
+        if (a.kv_out) reinterpret_cast<uint4*>(a.kv_out + m * N + key0)[v] = kv;
+        if (keep || write_value) vv[j] = load_kv8(a, m, N, val0 + 8 * v);
+        acc_sums(xv[j], kv, __ldg(reinterpret_cast<const uint4*>(qr) + v),
+                 __ldg(reinterpret_cast<const uint4*>(kr) + v), sh2, sk2, shwk);
+      }
     }
-    reinterpret_cast<uint4*>(orow)[v] = make_uint4(o[0], o[1], o[2], o[3]);
+    const float g = block_gate(a, m, s, sh2, sk2, shwk);
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const int v = threadIdx.x + j * kGateThreads;
+      if (v < nvec) {
+        if (write_value) reinterpret_cast<uint4*>(a.kv_out + m * N + val0)[v] = vv[j];
+        // a masked token's x passes through unchanged
+        reinterpret_cast<uint4*>(orow)[v] = keep ? gate_out8(xv[j], vv[j], g) : xv[j];
+      }
+    }
+  } else {
+    for (int v = threadIdx.x; v < nvec; v += kGateThreads) {
+      const uint4 kv = load_kv8(a, m, N, key0 + 8 * v);
+      if (a.kv_out) reinterpret_cast<uint4*>(a.kv_out + m * N + key0)[v] = kv;
+      acc_sums(__ldg(reinterpret_cast<const uint4*>(xr) + v), kv,
+               __ldg(reinterpret_cast<const uint4*>(qr) + v),
+               __ldg(reinterpret_cast<const uint4*>(kr) + v), sh2, sk2, shwk);
+    }
+    const float g = block_gate(a, m, s, sh2, sk2, shwk);
+    for (int v = threadIdx.x; v < nvec; v += kGateThreads) {
+      const uint4 xv = __ldg(reinterpret_cast<const uint4*>(xr) + v);
+      if (!keep && !write_value) {
+        reinterpret_cast<uint4*>(orow)[v] = xv;
+        continue;
+      }
+      const uint4 vv = load_kv8(a, m, N, val0 + 8 * v);
+      if (write_value) reinterpret_cast<uint4*>(a.kv_out + m * N + val0)[v] = vv;
+      reinterpret_cast<uint4*>(orow)[v] = keep ? gate_out8(xv, vv, g) : xv;
+    }
   }
 }
 
-cudaError_t launch_gate(const GateArgs& a, cudaStream_t st) {
-  const int64_t blocks = a.M * a.hc;
-  gate_kernel<<<static_cast<unsigned>(blocks), kGateThreads, 0, st>>>(a);
-  return cudaGetLastError();
+cudaError_t launch_gate(const GateArgs& a, cudaStream_t st, bool pdl) {
+  const dim3 grid(static_cast<unsigned>(a.M * a.hc)), block(kGateThreads);
+  const int nvec = a.dim / 8;
+  if (nvec <= 1 * kGateThreads) return launch_ex(gate_kernel<1>, grid, block, 0, st, pdl, a);
+  if (nvec <= 2 * kGateThreads) return launch_ex(gate_kernel<2>, grid, block, 0, st, pdl, a);
+  if (nvec <= 3 * kGateThreads) return launch_ex(gate_kernel<3>, grid, block, 0, st, pdl, a);
+  if (nvec <= 4 * kGateThreads) return launch_ex(gate_kernel<4>, grid, block, 0, st, pdl, a);
+  return launch_ex(gate_kernel<0>, grid, block, 0, st, pdl, a);
 }
 
 }  // namespace engram

@@ -71,6 +71,8 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
   volatile int* abort = &sh->abort;
+  pdl_wait();   // the activations come from the previous kernel of the stream
+  pdl_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0) {
@@ -172,7 +174,7 @@ int num_sms() {
 
 }  // namespace
 
-cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t st) {
+cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t st, bool pdl) {
   alignas(64) CUtensorMap tmA, tmB;
   if (!tensor_map_2d_bf16(&tmA, a.a, a.K, a.M, kBK, kBM)) return cudaErrorInvalidValue;
   if (!tensor_map_2d_bf16(&tmB, a.w, a.K, a.N, kBK, kBN)) return cudaErrorInvalidValue;
@@ -186,8 +188,8 @@ cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t st) {
   }
   const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
   const int grid = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
-  wkv_gemm_kernel<<<grid, kGemmThreads, smem, st>>>(tmA, tmB, a.kv, a.M, a.N, a.K, a.err);
-  return cudaGetLastError();
+  return launch_ex(wkv_gemm_kernel, dim3(grid), dim3(kGemmThreads), smem, st, pdl, tmA, tmB, a.kv,
+                   a.M, a.N, a.K, a.err);
 }
 
 }  // namespace engram

@@ -61,7 +61,7 @@ typedef enum engram_status {
  * Geometry of one Engram layer (Engram listing, __init__: dim, hc_mult, the layout's n_heads,
  * max_ngram_size, head_dim and num_embeddings; norm_eps is ModelArgs.norm_eps, whose value the
  * pages do not give). n_hash_cols = (max_ngram_size - 1) * n_heads rows are fetched per position.
- * Requirements: all sizes > 0; max_ngram_size >= 2; head_dim % 32 == 0 (one e8m0 scale per 32
+ * Requirements: all sizes > 0; 2 <= max_ngram_size <= 8; head_dim % 32 == 0 (one e8m0 scale per 32
  * elements); dim % 8 == 0; num_embeddings < 2^31; norm_eps >= 0.
  */
 typedef struct engram_desc {
@@ -200,8 +200,8 @@ ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
 /*
  * Bytes of scratch for engram_forward on M = B * T tokens with the fastest projection path (a
  * multiple of 256). engram_forward also accepts a smaller workspace and then runs the fastest
- * path that fits it; the smallest it accepts holds the hash ids and gathered rows (3,168 bytes
- * per token at the full geometry, rounded up to 256 twice).
+ * path that fits it; the smallest it accepts holds the gathered rows (3,072 bytes per token at
+ * the full geometry, rounded up to a multiple of 256).
  */
 ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64_t M);
 
@@ -239,8 +239,8 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
  * lives in a fixed array of ENGRAM_NOALLOC_SCRATCH_BYTES (8 MiB) that the library keeps in every
  * GPU that loads it, until the process exits. A call whose scratch would not fit returns
  * ENGRAM_EINVAL and launches nothing: at the full geometry (dim 5120, hc 4, 24 rows of
- * head_dim 64) that is more than 2,647 tokens (B * T) per call; geometries that take the unfused
- * path also keep the kv row there and fit far fewer tokens.
+ * head_dim 64) that is more than 2,730 tokens (B * T) per call. Within that limit the call runs
+ * the fastest projection path whose scratch fits in the array.
  *
  * This call allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. Its
  * first call on a device looks up the array's device address (cudaGetSymbolAddress, with that
