@@ -231,6 +231,8 @@ def run_native(args):
     # The dominant kernel, timed alone with CUDA events on the same stream: engram_wkv_gate (the
     # projection + gate kernel the step runs at this size) on the rows the step gathered.
     rows = ws[: M * geom.K * 2].view(torch.int16).view(M, geom.K)
+    kws = torch.empty(eg.api.engram_wkv_gate_workspace_size(desc, M), dtype=torch.uint8,
+                      device="cuda")
     kern_ms = []
     for i in range(args.steps):
         flush.zero_()
@@ -238,7 +240,7 @@ def run_native(args):
         a.record(stream)
         eg.engram_wkv_gate(desc, rows, weights.wkv, x.view(M, geom.hc_mult, geom.dim),
                            weights.q_weight, weights.k_weight, None,
-                           out.view(M, geom.hc_mult, geom.dim))
+                           out.view(M, geom.hc_mult, geom.dim), workspace=kws)
         b.record(stream)
         kern_ms.append((a, b))
     torch.cuda.synchronize()

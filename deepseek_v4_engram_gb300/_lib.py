@@ -56,7 +56,9 @@ SIGNATURES = {
     "engram_embed_rows": (ctypes.c_int, [_DESC, _P, _P, _P, _I64, _P, _P]),
     "engram_wkv": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P]),
     "engram_gate_and_add": (ctypes.c_int, [_DESC, _P, _P, _P, _P, _P, _P, _P, _I64, _P]),
-    "engram_wkv_gate": (ctypes.c_int, [_DESC, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P]),
+    "engram_wkv_gate_workspace_size": (_SZ, [_DESC, _I64]),
+    "engram_wkv_gate": (ctypes.c_int, [_DESC, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _P, _SZ,
+                                       _P]),
     "engram_forward_workspace_size": (_SZ, [_DESC, _I64]),
     "engram_forward": (ctypes.c_int, [_DESC, _TAB, _WTS, _P, _P, _I32, _I32, _P, _P, _I32, _P,
                                       _P, _P, _P, _P, _P, _SZ, _P]),

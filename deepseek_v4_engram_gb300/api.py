@@ -135,15 +135,24 @@ def engram_gate_and_add(desc, x, kv, q_weight, k_weight, token_mask, out, gate_o
                                      _ptr(gate_out, "f32", "gate_out"), M, _stream(stream)))
 
 
+def engram_wkv_gate_workspace_size(desc, M: int) -> int:
+    return int(lib().engram_wkv_gate_workspace_size(ctypes.byref(desc), M))
+
+
 def engram_wkv_gate(desc, rows, wkv, x, q_weight, k_weight, token_mask, out, gate_out=None,
-                    kv_out=None, stream=None):
+                    kv_out=None, workspace=None, stream=None):
+    """Stages 3 + 4 in one kernel. `workspace` (uint8 CUDA tensor) defaults to a fresh one."""
     M = x.shape[0]
+    if workspace is None:
+        workspace = torch.empty(max(engram_wkv_gate_workspace_size(desc, M), 256),
+                                dtype=torch.uint8, device=x.device)
     _check(lib().engram_wkv_gate(ctypes.byref(desc), _ptr(rows, "bf16", "rows"),
                                  _ptr(wkv, "bf16", "wkv"), _ptr(x, "bf16", "x"),
                                  _ptr(q_weight, "bf16", "q"), _ptr(k_weight, "bf16", "k"),
                                  _ptr(token_mask, "u8", "token_mask"), _ptr(out, "bf16", "out"),
                                  _ptr(gate_out, "f32", "gate_out"), _ptr(kv_out, "bf16", "kv_out"),
-                                 M, _stream(stream)))
+                                 M, _ptr(workspace, "u8", "workspace"), workspace.numel(),
+                                 _stream(stream)))
 
 
 def engram_forward_workspace_size(desc, M: int) -> int:

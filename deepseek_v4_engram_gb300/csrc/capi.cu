@@ -174,7 +174,7 @@ int forward_plans(const engram_desc_t* d, int64_t M, Plan* out) {
     out[n++] = {Path::kSmall, 1, base + kv_bytes};
   }
   if (!fused || M < kFusedMinTokens) out[n++] = {Path::kUnfused, 1, base + kv_bytes};
-  if (fused) out[n++] = {Path::kFused, 1, base};
+  if (fused) out[n++] = {Path::kFused, 1, base + fused_scratch_bytes(M, d->hc_mult)};
   if (fused && M >= kFusedMinTokens) out[n++] = {Path::kUnfused, 1, base + kv_bytes};
   return n;
 }
@@ -420,10 +420,16 @@ static FusedArgs make_fused_args(const engram_desc_t* desc, const uint16_t* rows
   return f;
 }
 
+ENGRAM_API size_t engram_wkv_gate_workspace_size(const engram_desc_t* desc, int64_t M) {
+  if (check_desc(desc) != ENGRAM_OK || M < 0) return 0;
+  return fused_scratch_bytes(M, desc->hc_mult);
+}
+
 ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
                                const uint16_t* wkv, const uint16_t* x, const uint16_t* q_weight,
                                const uint16_t* k_weight, const uint8_t* token_mask, uint16_t* out,
-                               float* gate_out, uint16_t* kv_out, int64_t M, void* stream) {
+                               float* gate_out, uint16_t* kv_out, int64_t M, void* workspace,
+                               size_t workspace_bytes, void* stream) {
   g_msg[0] = 0;
   int rc = gate_checks(desc, x, wkv, q_weight, k_weight, out, M);
   if (rc || M == 0) return rc;
@@ -432,15 +438,19 @@ ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
   if (!fused_supported(K, desc->hc_mult, desc->dim))
     return fail(ENGRAM_EUNSUPPORTED,
                 "engram_wkv_gate needs n_hash_cols * head_dim %% 64 == 0, dim %% 256 == 0, "
-                "hc_mult <= 8 and dim / hc_mult a multiple of 64; use engram_wkv + "
+                "dim <= 5120, hc_mult <= 8 and dim / hc_mult a multiple of 64; use engram_wkv + "
                 "engram_gate_and_add");
   if (!rows || !aligned(rows, 16)) return fail(ENGRAM_EINVAL, "rows must be 16-byte aligned");
   if (kv_out && !aligned(kv_out, 16)) return fail(ENGRAM_EINVAL, "kv_out must be 16-byte aligned");
+  const size_t need = fused_scratch_bytes(M, desc->hc_mult);
+  if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
+    return fail(ENGRAM_EINVAL, "workspace must be >= %zu bytes and 256-byte aligned", need);
   cudaError_t e;
   uint32_t* err = error_word(&e);
   if (!err) return cuda_fail(e, "engram_wkv_gate");
-  const FusedArgs f = make_fused_args(desc, rows, wkv, x, q_weight, k_weight, token_mask, out,
-                                      gate_out, kv_out, M, err);
+  FusedArgs f = make_fused_args(desc, rows, wkv, x, q_weight, k_weight, token_mask, out,
+                                gate_out, kv_out, M, err);
+  f.scratch = workspace;
   if ((e = launch_fused(f, static_cast<cudaStream_t>(stream))) != cudaSuccess)
     return cuda_fail(e, "engram_wkv_gate");
   return ENGRAM_OK;
@@ -523,6 +533,7 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
     FusedArgs f = make_fused_args(desc, rows, wts->wkv, x, wts->q_weight, wts->k_weight,
                                   token_mask, out, gate_out, kv_out, M, err);
     f.adv = adv;
+    f.scratch = ws;
     if ((e = launch_fused(f, st, true)) != cudaSuccess) return cuda_fail(e, "engram_forward: fused");
     return ENGRAM_OK;
   }

@@ -187,21 +187,28 @@ ENGRAM_API int engram_gate_and_add(const engram_desc_t* desc, const uint16_t* x,
  * so the kv row is never written to memory (unless kv_out is given).
  *   rows bf16 [M, n_hash_cols * head_dim] (the output of engram_embed_rows, flattened per token);
  *   wkv bf16 [dim * (hc + 1), n_hash_cols * head_dim]; x, q_weight, k_weight, token_mask, out,
- *   gate_out as in engram_gate_and_add; kv_out bf16 [M, dim * (hc + 1)] or NULL.
- * Results equal engram_wkv followed by engram_gate_and_add up to f32 summation order in the
- * gate. Requires n_hash_cols * head_dim % 64 == 0, dim % 256 == 0, hc_mult <= 8 and dim / hc_mult
- * a multiple of 64; otherwise returns ENGRAM_EUNSUPPORTED (use the two separate calls).
+ *   gate_out as in engram_gate_and_add; kv_out bf16 [M, dim * (hc + 1)] or NULL;
+ *   workspace: device scratch of at least engram_wkv_gate_workspace_size(desc, M) bytes,
+ *   256-byte aligned, not shared with a concurrent call (the gates the streams exchange).
+ * The kernel is a cooperative launch (all of its CTAs resident at once); a launch that cannot be
+ * co-resident returns ENGRAM_ECUDA. Results equal engram_wkv followed by engram_gate_and_add up
+ * to f32 summation order in the gate. Requires n_hash_cols * head_dim % 64 == 0, dim % 256 == 0,
+ * dim <= 5120, hc_mult <= 8 and dim / hc_mult a multiple of 64; otherwise returns
+ * ENGRAM_EUNSUPPORTED (use the two separate calls).
  */
+ENGRAM_API size_t engram_wkv_gate_workspace_size(const engram_desc_t* desc, int64_t M);
 ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
                                const uint16_t* wkv, const uint16_t* x, const uint16_t* q_weight,
                                const uint16_t* k_weight, const uint8_t* token_mask, uint16_t* out,
-                               float* gate_out, uint16_t* kv_out, int64_t M, void* stream);
+                               float* gate_out, uint16_t* kv_out, int64_t M, void* workspace,
+                               size_t workspace_bytes, void* stream);
 
 /*
  * Bytes of scratch for engram_forward on M = B * T tokens with the fastest projection path (a
  * multiple of 256). engram_forward also accepts a smaller workspace and then runs the fastest
- * path that fits it; the smallest it accepts holds the gathered rows (3,072 bytes per token at
- * the full geometry, rounded up to a multiple of 256).
+ * path that fits it; the smallest it accepts holds the gathered rows and the exchanged gates
+ * (3,088 bytes per token at the full geometry, plus 32 bytes per 256 tokens, each part rounded
+ * up to a multiple of 256).
  */
 ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64_t M);
 
@@ -239,7 +246,7 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
  * lives in a fixed array of ENGRAM_NOALLOC_SCRATCH_BYTES (8 MiB) that the library keeps in every
  * GPU that loads it, until the process exits. A call whose scratch would not fit returns
  * ENGRAM_EINVAL and launches nothing: at the full geometry (dim 5120, hc 4, 24 rows of
- * head_dim 64) that is more than 2,730 tokens (B * T) per call. Within that limit the call runs
+ * head_dim 64) that is more than 2,716 tokens (B * T) per call. Within that limit the call runs
  * the fastest projection path whose scratch fits in the array.
  *
  * This call allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. Its
