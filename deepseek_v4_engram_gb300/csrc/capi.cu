@@ -147,8 +147,8 @@ constexpr size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 //  - kSmall:   M <= 256: weight-streaming projection over every SM (split-K partials in f32 when
 //              the workspace holds them, else bf16 kv), then the gate kernel;
 //  - kUnfused: the persistent projection GEMM into a bf16 kv, then the gate kernel; measured
-//              faster than the fused kernel below 4096 tokens, where the fused kernel's one
-//              cluster per 128 tokens leaves most SMs idle;
+//              faster than the fused kernel below 1024 tokens (too few items to fill the GPU
+//              past the fused kernel's cold start);
 //  - kFused:   projection + gate in one kernel; kv never touches HBM; least workspace.
 enum class Path { kSmall, kUnfused, kFused };
 struct Plan {
@@ -156,7 +156,7 @@ struct Plan {
   int ksplit;
   size_t bytes;
 };
-constexpr int64_t kFusedMinTokens = 4096;
+constexpr int64_t kFusedMinTokens = 1024;
 
 // Candidate plans in order of preference; returns how many were written.
 int forward_plans(const engram_desc_t* d, int64_t M, Plan* out) {
@@ -174,7 +174,7 @@ int forward_plans(const engram_desc_t* d, int64_t M, Plan* out) {
     out[n++] = {Path::kSmall, 1, base + kv_bytes};
   }
   if (!fused || M < kFusedMinTokens) out[n++] = {Path::kUnfused, 1, base + kv_bytes};
-  if (fused) out[n++] = {Path::kFused, 1, base + fused_scratch_bytes(M, d->hc_mult)};
+  if (fused) out[n++] = {Path::kFused, 1, base + fused_scratch_bytes(M, d->hc_mult, d->dim)};
   if (fused && M >= kFusedMinTokens) out[n++] = {Path::kUnfused, 1, base + kv_bytes};
   return n;
 }
@@ -422,7 +422,7 @@ static FusedArgs make_fused_args(const engram_desc_t* desc, const uint16_t* rows
 
 ENGRAM_API size_t engram_wkv_gate_workspace_size(const engram_desc_t* desc, int64_t M) {
   if (check_desc(desc) != ENGRAM_OK || M < 0) return 0;
-  return fused_scratch_bytes(M, desc->hc_mult);
+  return fused_scratch_bytes(M, desc->hc_mult, desc->dim);
 }
 
 ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
@@ -438,11 +438,10 @@ ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
   if (!fused_supported(K, desc->hc_mult, desc->dim))
     return fail(ENGRAM_EUNSUPPORTED,
                 "engram_wkv_gate needs n_hash_cols * head_dim %% 64 == 0, dim %% 256 == 0, "
-                "dim <= 5120, hc_mult <= 8 and dim / hc_mult a multiple of 64; use engram_wkv + "
-                "engram_gate_and_add");
+                "dim <= 5120 and hc_mult <= 8; use engram_wkv + engram_gate_and_add");
   if (!rows || !aligned(rows, 16)) return fail(ENGRAM_EINVAL, "rows must be 16-byte aligned");
   if (kv_out && !aligned(kv_out, 16)) return fail(ENGRAM_EINVAL, "kv_out must be 16-byte aligned");
-  const size_t need = fused_scratch_bytes(M, desc->hc_mult);
+  const size_t need = fused_scratch_bytes(M, desc->hc_mult, desc->dim);
   if (workspace == nullptr || workspace_bytes < need || !aligned(workspace, 256))
     return fail(ENGRAM_EINVAL, "workspace must be >= %zu bytes and 256-byte aligned", need);
   cudaError_t e;

@@ -4,31 +4,39 @@
 // Engram listing, forward: kv = wkv(rows); key, value = split(kv); per (token, stream) the three
 // sums over dim (h^2, key^2, h*w*key) give the gate; out = bf16(h + gate * value).
 //
-// Work split. Tokens come in tiles of 256. For each tile and each stream s there is one CTA pair
-// (a 2-CTA cluster): CTA h of the pair owns tokens [128h, 128h + 128) of the tile. Together the
-// pair runs the projection as CTA-pair MMAs (tcgen05 cta_group::2, M = 256): each CTA stages its
-// 128 rows of the gathered activations and half of the 256 wkv rows of a tile per K-block, and
-// receives its 128 x 256 accumulator in its own TMEM. This halves the shared-memory operand
-// traffic per SM of a single-CTA 128 x 256 MMA. The even CTA issues the MMAs; both CTAs' TMA
+// Work split. The kernel is persistent: as many CTA pairs (2-CTA clusters) as fit on the GPU at
+// once, one CTA per SM. The work is cut into items of 256 tokens times one
+// column tile of kv: a key tile (256 key columns of one stream) or a value tile (256 value
+// columns, shared by every stream). Pairs take items from a global counter in the order of
+// fused_schedule.cuh, so every SM stays busy to the end whatever the token count, and a pair that
+// runs slow simply takes fewer items.
+//
+// Each item is a CTA-pair MMA (tcgen05 cta_group::2, M = 256): CTA h of the pair stages rows
+// [128h, 128h + 128) of the 256 tokens and half of the tile's wkv rows per K-block, and gets its
+// 128-row half of the accumulator in its own TMEM. The even CTA issues the MMAs; both CTAs' TMA
 // loads count on its barriers and its commits arrive on the barriers of both.
 //
-// Pair s computes stream s's dim / 256 key tiles and accumulates sum h^2, sum key^2 and
-// sum h*w*key for its tokens on its own (no partial sums cross CTAs). Each CTA then publishes its
-// 128 gates to global memory with a release flag, and waits (bounded) for the gates of the other
-// streams' pairs of the same tokens. Pair s then computes its share [s*dim/hc, (s+1)*dim/hc) of
-// the value columns and writes out[m, s', cols] = h + gate[m, s'] * value for every stream s'.
-// The pairs that exchange gates must run at the same time: the kernel is a cooperative launch
-// (co-residency guaranteed) with a persistent loop over token tiles.
+// Key item epilogue: per token, the three sums over the tile's 256 columns, written to a partial
+// buffer. The gate warp then counts the tile in (an atomic per token tile, half and stream); the
+// CTA that completes the last key tile of (token tile, half, stream) adds the partial sums in
+// column order (so the result does not depend on which pair ran what), forms the gates, and
+// publishes them with a release flag. Value item epilogue: wait (bounded) for the flags of every
+// stream of its tokens, then out[m, s, cols] = h + gate[m, s] * value for every stream s, computed
+// in place in the x box in shared memory and written back with a TMA store.
 //
-// Roles per CTA (352 threads):
-//   warp 0       TMA producer of this CTA's half of the GEMM operands, 4-stage ring;
+// Roles per CTA (384 threads):
+//   warp 0       TMA producer of this CTA's half of the GEMM operands, 5-stage ring; in the even
+//                CTA it also takes the items from the global counter and hands them to both CTAs
+//                through a small item ring in shared memory;
 //   warp 1       TMEM owner; in the even CTA also the MMA issuer (two 256-column accumulators);
 //   warps 2-9    epilogue: two warps per TMEM lane quadrant (warp w reads lanes 32*(w%4)...),
 //                thread = (token row, half of each 64-column box): tcgen05.ld, gate sums, output;
 //   warp 10      TMA producer of the residual streams x: 128-token x 64-column boxes into a
-//                3-slot ring, in exactly the order the epilogue consumes them.
-// w = q_weight[s] * k_weight[s] (f32, exact) is staged in shared memory once per CTA.
+//                3-slot ring, in exactly the order the epilogue consumes them;
+//   warp 11      gate warp: counts each key tile in and, for the last one, forms and publishes the
+//                gates, off the epilogue's path.
 #include "device.cuh"
+#include "fused_schedule.cuh"
 #include "kernels.h"
 #include "wkv_tiles.cuh"
 
@@ -39,17 +47,22 @@ namespace {
 constexpr int kEpiWarps = 8;
 constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kXWarp = 2 + kEpiWarps;
-constexpr int kFusedThreads = (kXWarp + 1) * 32;
-constexpr int kFusedStages = 4;            // A/B ring depth
+constexpr int kGateWarp = kXWarp + 1;
+constexpr int kFusedThreads = (kGateWarp + 1) * 32;
+constexpr int kFusedStages = 5;            // A/B ring depth
 constexpr int kPairB = kBN / 2;            // wkv rows of a key tile staged by each CTA of a pair
 constexpr int kStageABytes = kBM * kBK * 2;
 constexpr int kStageBBytes = kPairB * kBK * 2;
 constexpr int kXSlots = 3;                 // x ring depth
 constexpr int kXCols = 64;                 // columns per x box (128 B per row: one swizzle row)
 constexpr int kXBoxBytes = kBM * kXCols * 2;
+constexpr int kItemSlots = 4;              // item ring depth
+// readers of an item slot: MMA issuer, x producer, gate warp and 8 epilogue warps in the even
+// CTA; operand producer, x producer, gate warp and 8 epilogue warps in the odd CTA
+constexpr int kItemReaders = 2 * (3 + kEpiWarps);
 constexpr int kMaxHc = 8;
-constexpr int kMaxFusedDim = 5120;         // w tile in shared memory: dim floats
-constexpr int kTokensPerTile = 2 * kBM;    // tokens per pair
+constexpr int kMaxFusedDim = 5120;
+constexpr int kTokensPerTile = 2 * kBM;    // tokens per item
 constexpr uint32_t kEpiBarrier = 1;        // named barrier of the epilogue warps
 
 struct FusedShared {
@@ -59,15 +72,20 @@ struct FusedShared {
   uint64_t tempty[2];             // even CTA: both CTAs' epilogues released the accumulator
   uint64_t xfull[kXSlots];
   uint64_t xempty[kXSlots];
+  uint64_t ifull[kItemSlots];     // both CTAs: item index written (by the even CTA's producer)
+  uint64_t iempty[kItemSlots];    // even CTA: every reader of both CTAs has read the slot
+  uint64_t pfull[2];              // a key tile's partial sums are in global memory (128 arrivals)
+  uint64_t pempty[2];             // the gate warp has taken them
   uint64_t drain;
+  int32_t item[kItemSlots];       // item index, or -1: no more items
   uint32_t tmem_base;
   int abort;
-  float part[3][kBM];             // second-half partial sums, handed to the first half
+  float part[2][3][kBM];          // second-half partial sums, handed to the first half
 };
 
-size_t fused_smem_bytes(int dim) {
+size_t fused_smem_bytes() {
   return size_t(kFusedStages) * (kStageABytes + kStageBBytes) + size_t(kXSlots) * kXBoxBytes +
-         size_t(dim) * sizeof(float) + sizeof(FusedShared) + 1024;
+         sizeof(FusedShared) + 1024;
 }
 
 struct FusedParams {
@@ -77,24 +95,18 @@ struct FusedParams {
   uint16_t* out;
   float* gate_out;
   uint16_t* kv_out;
-  float* gx;          // [M, hc] gates, exchanged between the streams' pairs
-  int32_t* flags;     // [tiles, 2, hc] set to 1 once a CTA's gates are in gx; zero at launch
+  float* gx;          // [M, hc] gates, exchanged between pairs
+  float* part;        // [m_tiles, 2, hc, nk, 3, 128] per-key-tile partial sums
+  int32_t* next;      // item counter; zero at launch
+  int32_t* count;     // [m_tiles, 2, hc] key tiles done; zero at launch
+  int32_t* flags;     // [m_tiles, 2, hc] 1 once the gates are in gx; zero at launch
   int64_t M;
-  int32_t K, hc, dim, bnv, m_tiles;
+  int32_t K, hc, dim;
   float eps, inv_sqrt_dim;
   uint32_t* err;
   LenAdvance adv;
+  FusedSchedule sched;
 };
-
-// Value columns per stream are split into tiles of bnv columns: the largest multiple of 64 that
-// divides dim / hc and is at most 256 (each CTA of a pair stages bnv / 2 wkv rows).
-int value_tile_width(int32_t hc, int32_t dim) {
-  if (hc <= 0 || dim % hc != 0) return 0;
-  const int v = dim / hc;
-  for (int w = 256; w >= 64; w -= 64)
-    if (v % w == 0) return w;
-  return 0;
-}
 
 __device__ __forceinline__ float lo_bf16(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float hi_bf16(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -122,17 +134,29 @@ __device__ __forceinline__ void read_x_half_row(const uint8_t* box, int row, int
   }
 }
 
+__device__ __forceinline__ void write_x_half_row(uint8_t* box, int row, int half,
+                                                 const uint32_t (&v)[16]) {
+  const uint32_t base = smem_u32(box) + row * 128;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    sts128(base + (((4 * half + j) ^ (row & 7)) << 4),
+           make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+}
+
 // Consumer side of the x ring. release() hands a slot back to the x producer: the proxy fence
 // orders this thread's reads of the slot before the TMA load that will overwrite it.
 struct XRing {
   uint32_t slot = 0, phase = 0;
-  __device__ __forceinline__ void release(uint64_t* xempty) {
-    fence_proxy_async_shared();
-    mbar_arrive(&xempty[slot]);
+  __device__ __forceinline__ void advance() {
     if (++slot == kXSlots) {
       slot = 0;
       phase ^= 1u;
     }
+  }
+  __device__ __forceinline__ void release(uint64_t* xempty) {
+    fence_proxy_async_shared();
+    mbar_arrive(&xempty[slot]);
+    advance();
   }
 };
 
@@ -164,31 +188,80 @@ __device__ bool wait_flags(const int32_t* flags, int hc, volatile int* abort, ui
   return true;
 }
 
+// bar.red.or over the epilogue warps: a barrier that also tells every thread whether any of them
+// passed `pred`.
+__device__ __forceinline__ bool epi_any(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred)), "r"(kEpiBarrier), "r"(kEpiThreads)
+      : "memory");
+  return r != 0;
+}
+
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int32_t v) {
+  asm volatile("st.shared::cluster.b32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t* p, int32_t v) {
+  int32_t old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;"
+               : "=r"(old)
+               : "l"(p), "r"(v)
+               : "memory");
+  return old;
+}
+
+// Reader side of the item ring. next() waits (bounded) for the slot and reads the item; release()
+// tells the even CTA's producer that this reader is done with the slot.
+struct ItemReader {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ bool next(FusedShared* sh, int32_t& item, volatile int* abort,
+                                       uint32_t* err) {
+    if (!mbar_wait<true>(&sh->ifull[slot], phase, abort, err)) return false;
+    item = *reinterpret_cast<volatile int32_t*>(&sh->item[slot]);
+    return true;
+  }
+  __device__ __forceinline__ void advance() {
+    if (++slot == kItemSlots) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+  __device__ __forceinline__ void release(uint32_t iempty_leader0) {
+    mbar_arrive_remote(iempty_leader0 + slot * static_cast<uint32_t>(sizeof(uint64_t)));
+    advance();
+  }
+};
+
+// Column tile of wkv (in units of 256 rows) that an item multiplies with.
+__device__ __forceinline__ int32_t wkv_tile(const FusedItem& it, int32_t key_tiles) {
+  return it.value ? key_tiles + it.col : it.col;
+}
+
 __global__ void __launch_bounds__(kFusedThreads, 1)
     engram_fused_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmWk,
-                        const __grid_constant__ CUtensorMap tmWv,
-                        const __grid_constant__ CUtensorMap tmX, const FusedParams p) {
+                        const __grid_constant__ CUtensorMap tmW,
+                        const __grid_constant__ CUtensorMap tmX,
+                        const __grid_constant__ CUtensorMap tmOut, const FusedParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = sA + kFusedStages * kStageABytes;
   uint8_t* sX = sB + kFusedStages * kStageBBytes;
-  float* sW = reinterpret_cast<float*>(sX + kXSlots * kXBoxBytes);
-  FusedShared* sh = reinterpret_cast<FusedShared*>(sW + p.dim);
+  FusedShared* sh = reinterpret_cast<FusedShared*>(sX + kXSlots * kXBoxBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t half_m = static_cast<int32_t>(cluster_ctarank());   // which 128 tokens
   const bool leader = half_m == 0;                                   // issues the pair's MMAs
   const uint16_t pair_mask = 3u;
-  const int32_t s = static_cast<int32_t>(blockIdx.y);                // this pair's stream
-  const int32_t hc = p.hc, dim = p.dim, bnv = p.bnv;
-  const int32_t vcols = dim / hc;
-  const int nk = dim / kBN;                 // key tiles
-  const int nv = vcols / bnv;               // value tiles
-  const int ntiles = nk + nv;
+  const int32_t hc = p.hc, dim = p.dim;
+  const int32_t nk = dim / kBN;             // key tiles per stream (and value tiles)
+  const int32_t key_tiles = hc * nk;        // key tiles per token tile
   const int kblocks = p.K / kBK;
-  const int first_tile = static_cast<int>(blockIdx.z), tile_step = static_cast<int>(gridDim.z);
+  const FusedSchedule& sched = p.sched;
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kFusedStages; ++i) {
@@ -203,31 +276,34 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       mbar_init(&sh->tfull[a], 1);
       mbar_init(&sh->tempty[a], 2 * kEpiThreads);
     }
+    for (int i = 0; i < kItemSlots; ++i) {
+      mbar_init(&sh->ifull[i], 1);
+      mbar_init(&sh->iempty[i], kItemReaders);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&sh->pfull[i], kBM);
+      mbar_init(&sh->pempty[i], 1);
+    }
     mbar_init(&sh->drain, 1);
     sh->abort = 0;
     fence_mbar_init();
     tma_prefetch_desc(&tmA);
-    tma_prefetch_desc(&tmWk);
-    tma_prefetch_desc(&tmWv);
+    tma_prefetch_desc(&tmW);
     tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmOut);
   }
   if (warp == 1) {
     tmem_alloc_pair(&sh->tmem_base, kTmemCols);   // collectively with the other CTA of the pair
     tmem_relinquish_pair();
-  }
-  // w = q * k for this CTA's stream: a product of two bf16 values, exact in f32
-  for (int d = threadIdx.x; d < dim; d += kFusedThreads) {
-    const int64_t i = static_cast<int64_t>(s) * dim + d;
-    sW[d] = bf16_bits_to_f32(__ldg(p.q + i)) * bf16_bits_to_f32(__ldg(p.k + i));
   }
   tc_fence_before();
   cluster_sync_all();   // both CTAs' barriers initialised before any cross-CTA arrival
   tc_fence_after();
   const uint32_t tmem_base = sh->tmem_base;
   volatile int* abort = &sh->abort;
+  const uint32_t iempty_leader0 = map_to_rank(smem_u32(&sh->iempty[0]), 0);
   pdl_wait();   // rows (and the cache lengths) come from the previous kernel of the stream
-  if (p.adv.len != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 &&
-      threadIdx.x < 32)
+  if (p.adv.len != nullptr && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x < 32)
     for (int32_t b = threadIdx.x; b < p.adv.B; b += 32)
       p.adv.len[b] = min(p.adv.len[b] + p.adv.T, p.adv.cap);
 
@@ -236,25 +312,52 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     if (lane == 0) {
       TmaRingT<kFusedStages> ring;
       const uint32_t leader_bar0 = map_to_rank(smem_u32(&sh->full[0]), 0);
-      for (int mt = first_tile; mt < p.m_tiles && !*abort; mt += tile_step) {
-        const int32_t m0 = mt * kTokensPerTile + half_m * kBM;
-        for (int t = 0; t < ntiles && !*abort; ++t) {
-          const bool key = t < nk;
-          const int32_t nb = key ? kPairB : bnv / 2;          // wkv rows this CTA stages
-          const int32_t n0 = (key ? s * dim + t * kBN : hc * dim + s * vcols + (t - nk) * bnv) +
-                             half_m * nb;
-          const uint32_t bytes = static_cast<uint32_t>(kStageABytes + nb * kBK * 2);
-          for (int kb = 0; kb < kblocks; ++kb) {
-            if (!ring.acquire(sh->empty, abort, p.err)) break;
-            const uint32_t full_bar =
-                leader_bar0 + ring.stage * static_cast<uint32_t>(sizeof(uint64_t));
-            if (leader) mbar_arrive_expect_tx(&sh->full[ring.stage], 2 * bytes);
-            tma_load_2d_pair(sA + ring.stage * kStageABytes, &tmA, full_bar, kb * kBK, m0);
-            tma_load_2d_pair(sB + ring.stage * kStageBBytes, key ? &tmWk : &tmWv, full_bar,
-                             kb * kBK, n0);
-            ring.issued();
+      const uint32_t peer_item0 = map_to_rank(smem_u32(&sh->item[0]), 1);
+      const uint32_t peer_ifull0 = map_to_rank(smem_u32(&sh->ifull[0]), 1);
+      // every rows tile is read by (hc + 1) * dim / 256 items and every wkv tile by one item per
+      // token tile: keep them in L2 ahead of the streamed x and out
+      const uint64_t keep_l2 = l2_evict_last_policy();
+      ItemReader ir;   // the odd CTA reads its items; the even CTA writes both rings
+      uint32_t islot = 0, iphase = 0;
+      for (;;) {
+        int32_t idx;
+        if (leader) {
+          // the next item, taken only now (the operand ring still holds several K-blocks of the
+          // current one, which hides the atomic's latency), so that a pair holds few items
+          if (!mbar_wait<true>(&sh->iempty[islot], iphase ^ 1u, abort, p.err)) break;
+          const int32_t got = atomicAdd(p.next, 1);
+          idx = got < sched.items ? got : -1;
+          sh->item[islot] = idx;
+          st_cluster_s32(peer_item0 + islot * 4u, idx);
+          mbar_arrive(&sh->ifull[islot]);
+          mbar_arrive_remote(peer_ifull0 + islot * static_cast<uint32_t>(sizeof(uint64_t)));
+          if (++islot == kItemSlots) {
+            islot = 0;
+            iphase ^= 1u;
           }
+          if (idx < 0) break;
+        } else {
+          if (!ir.next(sh, idx, abort, p.err)) break;
+          ir.release(iempty_leader0);
+          if (idx < 0) break;
         }
+        const FusedItem it = fused_item_at(sched, idx);
+        const int32_t m0 = it.mt * kTokensPerTile + half_m * kBM;
+        const int32_t n0 = wkv_tile(it, key_tiles) * kBN + half_m * kPairB;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!ring.acquire(sh->empty, abort, p.err)) { ok = false; break; }
+          const uint32_t full_bar =
+              leader_bar0 + ring.stage * static_cast<uint32_t>(sizeof(uint64_t));
+          if (leader)
+            mbar_arrive_expect_tx(&sh->full[ring.stage], 2 * (kStageABytes + kStageBBytes));
+          tma_load_2d_pair_hint(sA + ring.stage * kStageABytes, &tmA, full_bar, kb * kBK, m0,
+                                keep_l2);
+          tma_load_2d_pair_hint(sB + ring.stage * kStageBBytes, &tmW, full_bar, kb * kBK, n0,
+                                keep_l2);
+          ring.issued();
+        }
+        if (!ok) break;
       }
       // the even CTA's full barriers count this CTA's loads; it waits on them for both
       if (leader) ring.drain(sh->full);
@@ -263,31 +366,31 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     // ------------------------------------------------------------- MMA issuer (even CTA)
     if (lane == 0 && leader) {
       uint32_t stage = 0, phase = 0, t_all = 0;
-      bool ok = true;
-      for (int mt = first_tile; mt < p.m_tiles && ok && !*abort; mt += tile_step) {
-        for (int t = 0; t < ntiles && ok && !*abort; ++t, ++t_all) {
-          const uint32_t acc = t_all & 1, acc_phase = (t_all >> 1) & 1;
-          if (!mbar_wait<true>(&sh->tempty[acc], acc_phase ^ 1u, abort, p.err)) {
-            ok = false;
-            break;
-          }
+      ItemReader ir;
+      const uint32_t idesc = idesc_bf16_f32(2 * kBM, kBN);
+      for (;; ++t_all) {
+        int32_t idx;
+        if (!ir.next(sh, idx, abort, p.err)) break;
+        ir.release(iempty_leader0);
+        if (idx < 0) break;
+        const uint32_t acc = t_all & 1, acc_phase = (t_all >> 1) & 1;
+        if (!mbar_wait<true>(&sh->tempty[acc], acc_phase ^ 1u, abort, p.err)) break;
+        tc_fence_after();
+        const uint32_t d = tmem_base + acc * kBN;
+        bool ok = true;
+        for (int kb = 0; kb < kblocks; ++kb) {
+          if (!mbar_wait(&sh->full[stage], phase, abort, p.err)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t d = tmem_base + acc * kBN;
-          const uint32_t idesc = idesc_bf16_f32(2 * kBM, t < nk ? kBN : bnv);
-          for (int kb = 0; kb < kblocks; ++kb) {
-            if (!mbar_wait(&sh->full[stage], phase, abort, p.err)) { ok = false; break; }
-            tc_fence_after();
-            const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + stage * kStageABytes));
-            const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * kStageBBytes));
+          const uint64_t ad = sw128_kmajor_desc(smem_u32(sA + stage * kStageABytes));
+          const uint64_t bd = sw128_kmajor_desc(smem_u32(sB + stage * kStageBBytes));
 #pragma unroll
-            for (int kk = 0; kk < kBK / kUmmaK; ++kk)
-              tc_mma_bf16_pair(d, ad + 2ull * kk, bd + 2ull * kk, idesc, (kb | kk) != 0);
-            tc_commit_pair_mc(&sh->empty[stage], pair_mask);
-            if (++stage == kFusedStages) { stage = 0; phase ^= 1u; }
-          }
-          if (!ok) break;
-          tc_commit_pair_mc(&sh->tfull[acc], pair_mask);
+          for (int kk = 0; kk < kBK / kUmmaK; ++kk)
+            tc_mma_bf16_pair(d, ad + 2ull * kk, bd + 2ull * kk, idesc, (kb | kk) != 0);
+          tc_commit_pair_mc(&sh->empty[stage], pair_mask);
+          if (++stage == kFusedStages) { stage = 0; phase ^= 1u; }
         }
+        if (!ok) break;
+        tc_commit_pair_mc(&sh->tfull[acc], pair_mask);
       }
       tc_commit_pair_mc(&sh->drain, pair_mask);
     }
@@ -296,34 +399,100 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     __syncwarp();
   } else if (warp == kXWarp) {
     // ------------------------------------------------------------- x producer
-    // Same order as the epilogue, per token tile: key tiles (stream s, 4 boxes each), then value
-    // tiles (for each 64-column box of the tile, the hc streams in turn).
+    // Same order as the epilogue: a key item takes its stream's 4 boxes; a value item, for each
+    // 64-column box of the tile, the hc streams in turn.
     if (lane == 0) {
       TmaRingT<kXSlots> ring;
-      const int steps = nk * (kBN / kXCols) + nv * (bnv / kXCols) * hc;
-      for (int mt = first_tile; mt < p.m_tiles && !*abort; mt += tile_step) {
-        const int32_t m0 = mt * kTokensPerTile + half_m * kBM;
-        for (int q = 0; q < steps && !*abort; ++q) {
+      ItemReader ir;
+      const uint64_t stream_l2 = l2_evict_first_policy();   // x: read by one key and one value item
+      bool ok = true;
+      while (ok) {
+        int32_t idx;
+        if (!ir.next(sh, idx, abort, p.err)) break;
+        ir.release(iempty_leader0);
+        if (idx < 0) break;
+        const FusedItem it = fused_item_at(sched, idx);
+        const int32_t m0 = it.mt * kTokensPerTile + half_m * kBM;
+        const int steps = it.value ? (kBN / kXCols) * hc : kBN / kXCols;
+        for (int q = 0; q < steps; ++q) {
           int32_t col, stream;
-          if (q < nk * (kBN / kXCols)) {
-            col = q * kXCols;
-            stream = s;
+          if (it.value) {
+            col = it.col * kBN + (q / hc) * kXCols;
+            stream = q % hc;
           } else {
-            const int v = q - nk * (kBN / kXCols);
-            col = s * vcols + (v / hc) * kXCols;
-            stream = v % hc;
+            col = (it.col % nk) * kBN + q * kXCols;
+            stream = it.col / nk;
           }
-          if (!ring.acquire(sh->xempty, abort, p.err)) break;
+          if (!ring.acquire(sh->xempty, abort, p.err)) { ok = false; break; }
           mbar_arrive_expect_tx(&sh->xfull[ring.stage], kXBoxBytes);
-          tma_load_3d(sX + ring.stage * kXBoxBytes, &tmX, &sh->xfull[ring.stage], col, stream,
-                      m0);
+          tma_load_3d_hint(sX + ring.stage * kXBoxBytes, &tmX, &sh->xfull[ring.stage], col,
+                           stream, m0, stream_l2);
           ring.issued();
         }
       }
       ring.drain(sh->xfull);
     }
+  } else if (warp == kGateWarp) {
+    // ------------------------------------------------------------- gate warp
+    // For every key tile this CTA finishes: count it in; if it was the last of its (token tile,
+    // half, stream), add the partial sums of all the stream's key tiles in column order, form
+    // the 128 gates and publish them.
+    ItemReader ir;
+    uint32_t nkey = 0;
+    for (;;) {
+      int32_t idx = -1;
+      bool ok = ir.next(sh, idx, abort, p.err);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      __syncwarp();
+      if (lane == 0) ir.release(iempty_leader0);
+      else ir.advance();
+      if (!ok || idx < 0) break;
+      const FusedItem it = fused_item_at(sched, idx);
+      if (it.value) continue;
+      const uint32_t b = nkey & 1, ph = (nkey >> 1) & 1;
+      ++nkey;
+      ok = mbar_wait(&sh->pfull[b], ph, abort, p.err);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (!ok) break;
+      const int32_t s = it.col / nk;
+      const int64_t ts = (static_cast<int64_t>(it.mt) * 2 + half_m) * hc + s;
+      int32_t last = 0;
+      if (lane == 0) {
+        __threadfence();   // the epilogue's partial sums (ordered before pfull) before the count
+        last = atom_add_acq_rel_gpu(p.count + ts, 1) == nk - 1;
+        mbar_arrive(&sh->pempty[b]);
+      }
+      last = __shfl_sync(0xFFFFFFFFu, last, 0);
+      if (!last) continue;
+      __threadfence();
+      const float* pp = p.part + ts * nk * 3 * kBM;
+      for (int r4 = 0; r4 < kBM / 32; ++r4) {
+        const int rr = r4 * 32 + lane;
+        const int64_t m = static_cast<int64_t>(it.mt) * kTokensPerTile + half_m * kBM + rr;
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f;
+        for (int j = 0; j < nk; ++j) {   // column order: independent of who ran what
+          const float* pj = pp + static_cast<int64_t>(j) * 3 * kBM;
+          a0 += __ldcg(pj + rr);
+          a1 += __ldcg(pj + kBM + rr);
+          a2 += __ldcg(pj + 2 * kBM + rr);
+        }
+        if (m < p.M) {
+          const bool keep = p.mask == nullptr || p.mask[m] != 0;
+          const float g = keep ? gate_from_sums(a0, a1, a2, dim, p.eps, p.inv_sqrt_dim) : 0.f;
+          p.gx[m * hc + s] = g;
+          if (p.gate_out) p.gate_out[m * hc + s] = g;
+        }
+      }
+      __syncwarp();
+      if (lane == 0) {
+        __threadfence();
+        st_release_gpu(p.flags + (static_cast<int64_t>(it.mt) * 2 + half_m) * hc + s, 1);
+      }
+    }
   } else {
     // ------------------------------------------------------------- epilogue (warps 2-9)
+    // Failed waits (abort) are made warp-uniform at once and epilogue-uniform at the barriers, so
+    // that every epilogue thread passes the same named barriers and leaves the loop together.
     const int quad = warp & 3;                       // TMEM lane quadrant
     const int half = (warp - 2) >> 2;                // which 32 columns of each 64-column box
     const int row = quad * 32 + lane;
@@ -331,128 +500,177 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const int64_t N = static_cast<int64_t>(dim) * (hc + 1);
     const uint32_t tempty_leader0 = map_to_rank(smem_u32(&sh->tempty[0]), 0);
     XRing xr;
-    uint32_t t_all = 0;
-    bool ok = true;
+    ItemReader ir;
+    uint32_t nkey = 0;
+    int32_t pending = -1;   // thread 64: x slot whose TMA store may still be reading it
 
-    for (int mt = first_tile; mt < p.m_tiles && ok; mt += tile_step) {
-      const int64_t m = static_cast<int64_t>(mt) * kTokensPerTile + half_m * kBM + row;
+    for (uint32_t t_all = 0;; ++t_all) {
+      int32_t idx = -1;
+      bool ok = ir.next(sh, idx, abort, p.err);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      __syncwarp();   // one arrival per warp, after every lane has read the item
+      if (lane == 0) ir.release(iempty_leader0);
+      else ir.advance();
+      if (epi_any(!ok || idx < 0)) break;
+
+      const FusedItem it = fused_item_at(sched, idx);
+      const int64_t m = static_cast<int64_t>(it.mt) * kTokensPerTile + half_m * kBM + row;
       const bool valid = m < p.M;
       const bool keep = valid && (p.mask == nullptr || p.mask[m] != 0);
-      // two accumulators per sum shorten the dependent FMA chains
-      float sh2[2] = {0.f, 0.f}, sk2[2] = {0.f, 0.f}, shwk[2] = {0.f, 0.f};
+      int32_t* fl = p.flags + (static_cast<int64_t>(it.mt) * 2 + half_m) * hc;
       float gl[kMaxHc];
 #pragma unroll
       for (int i = 0; i < kMaxHc; ++i) gl[i] = 0.f;
-
-      for (int t = 0; t < ntiles && ok; ++t, ++t_all) {
-        const uint32_t acc = t_all & 1, acc_phase = (t_all >> 1) & 1;
-        if (!mbar_wait(&sh->tfull[acc], acc_phase, abort, p.err)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t tbase = tmem_base + lane_base + acc * kBN + half * 32;
-        if (t < nk) {
-          // key tile: columns d0 .. d0 + 255 of stream s, in four 64-column boxes
-          for (int c4 = 0; c4 < kBN / kXCols; ++c4) {
-            const int32_t d = t * kBN + c4 * kXCols + half * 32;   // first column of this half
-            uint32_t r[32];
-            tc_ld_32x32b_x32(tbase + c4 * kXCols, r);
-            if (!mbar_wait(&sh->xfull[xr.slot], xr.phase, abort, p.err)) { ok = false; break; }
-            uint32_t xv[16];
-            read_x_half_row(sX + xr.slot * kXBoxBytes, row, half, xv);
-            xr.release(sh->xempty);
-            tc_wait_ld(r);
-            uint32_t kb16[16];
+      if (it.value) {
+        // the gates of every stream of these tokens (bounded wait)
+        bool got = true;
+        if (threadIdx.x == 64) got = wait_flags(fl, hc, abort, p.err);
+        if (epi_any(!got)) break;
+        if (valid) {
+          ld_acquire_gpu(fl);   // this thread's own acquire of the published gates
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              kb16[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-              const float2 w2 = *reinterpret_cast<const float2*>(sW + d + 2 * e);
-              const float key0 = lo_bf16(kb16[e]), key1 = hi_bf16(kb16[e]);
-              const float h0 = lo_bf16(xv[e]), h1 = hi_bf16(xv[e]);
-              sh2[0] = fmaf(h0, h0, sh2[0]);
-              sk2[0] = fmaf(key0, key0, sk2[0]);
-              shwk[0] = fmaf(h0 * w2.x, key0, shwk[0]);
-              sh2[1] = fmaf(h1, h1, sh2[1]);
-              sk2[1] = fmaf(key1, key1, sk2[1]);
-              shwk[1] = fmaf(h1 * w2.y, key1, shwk[1]);
-            }
-            if (valid && p.kv_out)
-              store_words<16>(p.kv_out + m * N + static_cast<int64_t>(s) * dim + d, kb16);
-          }
-        } else {
-          // value tile: value columns col0 .. col0 + bnv - 1, shared by all hc streams
-          const int32_t col0 = s * vcols + (t - nk) * bnv;
-          for (int c4 = 0; c4 < bnv / kXCols && ok; ++c4) {
-            const int32_t col = col0 + c4 * kXCols + half * 32;
-            uint32_t r[32];
-            tc_ld_32x32b_x32(tbase + c4 * kXCols, r);
-            tc_wait_ld(r);
-            uint32_t vb[16];
-#pragma unroll
-            for (int e = 0; e < 16; ++e)
-              vb[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-            if (valid && p.kv_out)
-              store_words<16>(p.kv_out + m * N + static_cast<int64_t>(hc) * dim + col, vb);
-            for (int s2 = 0; s2 < hc; ++s2) {
-              if (!mbar_wait(&sh->xfull[xr.slot], xr.phase, abort, p.err)) { ok = false; break; }
-              uint32_t xv[16];
-              read_x_half_row(sX + xr.slot * kXBoxBytes, row, half, xv);
-              xr.release(sh->xempty);
-              if (!valid) continue;
-              if (keep) {
-                float g = gl[0];
-#pragma unroll
-                for (int i = 1; i < kMaxHc; ++i) g = (s2 == i) ? gl[i] : g;
-#pragma unroll
-                for (int e = 0; e < 16; ++e)
-                  xv[e] = pack_bf16x2(fmaf(g, lo_bf16(vb[e]), lo_bf16(xv[e])),
-                                      fmaf(g, hi_bf16(vb[e]), hi_bf16(xv[e])));
-              }   // a masked token's x passes through unchanged
-              store_words<16>(p.out + (m * hc + s2) * dim + col, xv);
-            }
-          }
-        }
-        if (!ok) break;
-        // hand the accumulator back to the pair's MMA issuer
-        tc_fence_before();
-        mbar_arrive_remote(tempty_leader0 + acc * static_cast<uint32_t>(sizeof(uint64_t)));
-
-        if (t == nk - 1) {
-          // all key tiles done. The second half hands its partial sums to the first; the first
-          // half forms the gates of this CTA's 128 tokens and publishes them; then everyone
-          // waits for the gates of every stream for these tokens.
-          const float a0 = sh2[0] + sh2[1], a1 = sk2[0] + sk2[1], a2 = shwk[0] + shwk[1];
-          if (half == 1) {
-            sh->part[0][row] = a0;
-            sh->part[1][row] = a1;
-            sh->part[2][row] = a2;
-          }
-          named_bar_sync(kEpiBarrier, kEpiThreads);
-          if (half == 0) {
-            float g = 0.f;
-            if (keep)
-              g = gate_from_sums(a0 + sh->part[0][row], a1 + sh->part[1][row],
-                                 a2 + sh->part[2][row], dim, p.eps, p.inv_sqrt_dim);
-            if (valid) {
-              p.gx[m * hc + s] = g;
-              if (p.gate_out) p.gate_out[m * hc + s] = g;
-            }
-          }
-          int32_t* fl = p.flags + (static_cast<int64_t>(mt) * 2 + half_m) * hc;
-          named_bar_sync(kEpiBarrier, kEpiThreads);   // every gate of this CTA is written
-          if (threadIdx.x == 64) {
-            __threadfence();
-            st_release_gpu(fl + s, 1);
-            wait_flags(fl, hc, abort, p.err);
-          }
-          named_bar_sync(kEpiBarrier, kEpiThreads);   // every stream's gates are visible
-          if (*abort) { ok = false; break; }
-          if (valid) {
-            ld_acquire_gpu(fl);   // this thread's own acquire of the published gates
-#pragma unroll
-            for (int i = 0; i < kMaxHc; ++i) gl[i] = i < hc ? __ldcg(p.gx + m * hc + i) : 0.f;
-          }
+          for (int i = 0; i < kMaxHc; ++i) gl[i] = i < hc ? __ldcg(p.gx + m * hc + i) : 0.f;
         }
       }
+
+      const uint32_t acc = t_all & 1, acc_phase = (t_all >> 1) & 1;
+      ok = mbar_wait(&sh->tfull[acc], acc_phase, abort, p.err);
+      ok = __all_sync(0xFFFFFFFFu, ok);
+      if (ok) tc_fence_after();
+      const uint32_t tbase = tmem_base + lane_base + acc * kBN + half * 32;
+      float sh2[2] = {0.f, 0.f}, sk2[2] = {0.f, 0.f}, shwk[2] = {0.f, 0.f};
+      const int32_t s = it.col / nk;                 // key item: its stream
+      if (!it.value) {
+        // key tile: columns d0 .. d0 + 255 of stream s, in four 64-column boxes
+        for (int c4 = 0; c4 < kBN / kXCols && ok; ++c4) {
+          const int32_t d = (it.col % nk) * kBN + c4 * kXCols + half * 32;   // this half's columns
+          uint32_t r[32];
+          tc_ld_32x32b_x32(tbase + c4 * kXCols, r);
+          // w = q * k for these 32 columns: the same for every lane (a product of two bf16
+          // values, exact in f32)
+          uint32_t qv[16], kv[16];
+          const uint4* qp = reinterpret_cast<const uint4*>(p.q + static_cast<int64_t>(s) * dim + d);
+          const uint4* kp = reinterpret_cast<const uint4*>(p.k + static_cast<int64_t>(s) * dim + d);
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const uint4 a = __ldg(qp + j), b = __ldg(kp + j);
+            qv[4 * j] = a.x; qv[4 * j + 1] = a.y; qv[4 * j + 2] = a.z; qv[4 * j + 3] = a.w;
+            kv[4 * j] = b.x; kv[4 * j + 1] = b.y; kv[4 * j + 2] = b.z; kv[4 * j + 3] = b.w;
+          }
+          ok = mbar_wait(&sh->xfull[xr.slot], xr.phase, abort, p.err);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          uint32_t xv[16];
+          if (ok) read_x_half_row(sX + xr.slot * kXBoxBytes, row, half, xv);
+          xr.release(sh->xempty);
+          tc_wait_ld(r);
+          if (!ok) break;
+          uint32_t kb16[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            kb16[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+            const float w0 = lo_bf16(qv[e]) * lo_bf16(kv[e]);
+            const float w1 = hi_bf16(qv[e]) * hi_bf16(kv[e]);
+            const float key0 = lo_bf16(kb16[e]), key1 = hi_bf16(kb16[e]);
+            const float h0 = lo_bf16(xv[e]), h1 = hi_bf16(xv[e]);
+            sh2[0] = fmaf(h0, h0, sh2[0]);
+            sk2[0] = fmaf(key0, key0, sk2[0]);
+            shwk[0] = fmaf(h0 * w0, key0, shwk[0]);
+            sh2[1] = fmaf(h1, h1, sh2[1]);
+            sk2[1] = fmaf(key1, key1, sk2[1]);
+            shwk[1] = fmaf(h1 * w1, key1, shwk[1]);
+          }
+          if (valid && p.kv_out)
+            store_words<16>(p.kv_out + m * N + static_cast<int64_t>(s) * dim + d, kb16);
+        }
+      } else {
+        // value tile: value columns col0 .. col0 + 255, shared by all hc streams. Each (64-column
+        // box, stream) is computed in place in its x slot and written out by one TMA store; the
+        // slot goes back to the x producer once the store has read it.
+        const int32_t col0 = it.col * kBN;
+        const int32_t m0 = it.mt * kTokensPerTile + half_m * kBM;
+        for (int c4 = 0; c4 < kBN / kXCols && ok; ++c4) {
+          const int32_t colb = col0 + c4 * kXCols;
+          uint32_t r[32];
+          tc_ld_32x32b_x32(tbase + c4 * kXCols, r);
+          tc_wait_ld(r);
+          uint32_t vb[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            vb[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+          if (valid && p.kv_out)
+            store_words<16>(p.kv_out + m * N + static_cast<int64_t>(hc) * dim + colb + half * 32,
+                            vb);
+          for (int s2 = 0; s2 < hc; ++s2) {
+            ok = mbar_wait(&sh->xfull[xr.slot], xr.phase, abort, p.err);
+            ok = __all_sync(0xFFFFFFFFu, ok);
+            uint8_t* box = sX + xr.slot * kXBoxBytes;
+            if (ok && keep) {   // a masked token's x passes through unchanged
+              float g = gl[0];
+#pragma unroll
+              for (int i = 1; i < kMaxHc; ++i) g = (s2 == i) ? gl[i] : g;
+              uint32_t xv[16];
+              read_x_half_row(box, row, half, xv);
+#pragma unroll
+              for (int e = 0; e < 16; ++e)
+                xv[e] = pack_bf16x2(fmaf(g, lo_bf16(vb[e]), lo_bf16(xv[e])),
+                                    fmaf(g, hi_bf16(vb[e]), hi_bf16(xv[e])));
+              write_x_half_row(box, row, half, xv);
+            }
+            fence_proxy_async_shared();   // the box's writes, before the TMA store reads them
+            const bool fail = epi_any(!ok);
+            if (threadIdx.x == 64) {
+              if (!fail) {
+                tma_store_3d(&tmOut, box, colb, s2, m0);
+                bulk_commit_group();
+              }
+              bulk_wait_group_read<1>();   // every store but this one has read its slot
+              if (pending >= 0) mbar_arrive(&sh->xempty[pending]);
+              pending = static_cast<int32_t>(xr.slot);
+            } else {
+              mbar_arrive(&sh->xempty[xr.slot]);
+            }
+            xr.advance();
+            if (fail) {
+              ok = false;
+              break;
+            }
+          }
+        }
+        if (threadIdx.x == 64 && pending >= 0) {
+          bulk_wait_group_read<0>();
+          mbar_arrive(&sh->xempty[pending]);
+          pending = -1;
+        }
+      }
+      // hand the accumulator back to the pair's MMA issuer
+      tc_fence_before();
+      mbar_arrive_remote(tempty_leader0 + acc * static_cast<uint32_t>(sizeof(uint64_t)));
+
+      if (!it.value) {
+        // The key tile's sums: the second half hands its partial sums to the first, which writes
+        // this CTA's 128 rows of them to the partial buffer and hands the tile to the gate warp.
+        const uint32_t b = nkey & 1, ph = (nkey >> 1) & 1;
+        ++nkey;
+        if (half == 1) {
+          sh->part[b][0][row] = sh2[0] + sh2[1];
+          sh->part[b][1][row] = sk2[0] + sk2[1];
+          sh->part[b][2][row] = shwk[0] + shwk[1];
+        }
+        if (epi_any(!ok)) break;
+        if (half == 0) {
+          const int64_t ts = (static_cast<int64_t>(it.mt) * 2 + half_m) * hc + s;
+          float* pj = p.part + (ts * nk + it.col % nk) * 3 * kBM;
+          __stcg(pj + row, sh2[0] + sh2[1] + sh->part[b][0][row]);
+          __stcg(pj + kBM + row, sk2[0] + sk2[1] + sh->part[b][1][row]);
+          __stcg(pj + 2 * kBM + row, shwk[0] + shwk[1] + sh->part[b][2][row]);
+          ok = mbar_wait(&sh->pempty[b], ph ^ 1u, abort, p.err);
+          ok = __all_sync(0xFFFFFFFFu, ok);
+          if (ok) mbar_arrive(&sh->pfull[b]);
+        }
+      }
+      if (epi_any(!ok)) break;
     }
+    if (threadIdx.x == 64) bulk_wait_group<0>();   // the output stores are complete
   }
 
   // The pair's TMEM is released by both CTAs together, so neither may do so while the other
@@ -473,7 +691,7 @@ int max_resident_pairs() {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(2, 1, 1);
     cfg.blockDim = dim3(kFusedThreads, 1, 1);
-    cfg.dynamicSmemBytes = fused_smem_bytes(kMaxFusedDim);
+    cfg.dynamicSmemBytes = fused_smem_bytes();
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 2;
@@ -491,42 +709,61 @@ int max_resident_pairs() {
 
 size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
+struct ScratchLayout {
+  size_t gx, part, sync, sync_bytes, total;
+};
+
+// gx [M, hc] f32 | partial sums [m_tiles, 2, hc, nk, 3, 128] f32 |
+// item counter, then count and flags [m_tiles, 2, hc] each (int32, cleared before each launch)
+ScratchLayout scratch_layout(int64_t M, int32_t hc, int32_t dim) {
+  const int64_t m_tiles = (M + kTokensPerTile - 1) / kTokensPerTile;
+  ScratchLayout l{};
+  l.gx = 0;
+  l.part = round256(size_t(M) * hc * 4);
+  l.sync = l.part + round256(size_t(m_tiles) * 2 * hc * (dim / kBN) * 3 * kBM * 4);
+  l.sync_bytes = (1 + size_t(m_tiles) * 2 * hc * 2) * 4;
+  l.total = l.sync + round256(l.sync_bytes);
+  return l;
+}
+
 }  // namespace
 
 bool fused_supported(int32_t K, int32_t hc, int32_t dim) {
   return K > 0 && K % kBK == 0 && hc >= 1 && hc <= kMaxHc && dim % kBN == 0 &&
-         dim <= kMaxFusedDim && value_tile_width(hc, dim) > 0;
+         dim <= kMaxFusedDim;
 }
 
-size_t fused_scratch_bytes(int64_t M, int32_t hc) {
-  const int64_t tiles = (M + kTokensPerTile - 1) / kTokensPerTile;
-  return round256(size_t(M) * hc * 4) + round256(size_t(tiles) * 2 * hc * 4);
+size_t fused_scratch_bytes(int64_t M, int32_t hc, int32_t dim) {
+  return scratch_layout(M, hc, dim).total;
 }
 
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool /*pdl*/) {
-  const int bnv = value_tile_width(a.hc, a.dim);
   const int64_t N = static_cast<int64_t>(a.dim) * (a.hc + 1);
   const int64_t m_tiles = (a.M + kTokensPerTile - 1) / kTokensPerTile;
-  alignas(64) CUtensorMap tmA, tmWk, tmWv, tmX;
+  alignas(64) CUtensorMap tmA, tmW, tmX, tmOut;
   if (!tensor_map_2d_bf16(&tmA, a.a, a.K, a.M, kBK, kBM) ||
-      !tensor_map_2d_bf16(&tmWk, a.w, a.K, N, kBK, kPairB) ||
-      !tensor_map_2d_bf16(&tmWv, a.w, a.K, N, kBK, bnv / 2) ||
-      !tensor_map_3d_bf16(&tmX, a.x, a.dim, a.hc, a.M, kXCols, 1, kBM))
+      !tensor_map_2d_bf16(&tmW, a.w, a.K, N, kBK, kPairB) ||
+      !tensor_map_3d_bf16(&tmX, a.x, a.dim, a.hc, a.M, kXCols, 1, kBM) ||
+      !tensor_map_3d_bf16(&tmOut, a.out, a.dim, a.hc, a.M, kXCols, 1, kBM))
     return cudaErrorInvalidValue;
   static bool attr_set = false;
   if (!attr_set) {
     cudaError_t e = cudaFuncSetAttribute(engram_fused_kernel,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(fused_smem_bytes(kMaxFusedDim)));
+                                         static_cast<int>(fused_smem_bytes()));
     if (e != cudaSuccess) return e;
     attr_set = true;
   }
-  // scratch: the exchanged gates, then the flags (cleared before the launch)
-  float* gx = static_cast<float*>(a.scratch);
-  int32_t* flags = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(a.scratch) +
-                                              round256(size_t(a.M) * a.hc * 4));
-  cudaError_t e = cudaMemsetAsync(flags, 0, size_t(m_tiles) * 2 * a.hc * 4, st);
+  const ScratchLayout l = scratch_layout(a.M, a.hc, a.dim);
+  uint8_t* base = static_cast<uint8_t*>(a.scratch);
+  int32_t* sync = reinterpret_cast<int32_t*>(base + l.sync);
+  cudaError_t e = cudaMemsetAsync(sync, 0, l.sync_bytes, st);
   if (e != cudaSuccess) return e;
+
+  const int32_t nk = a.dim / kBN;
+  const int64_t items = m_tiles * (int64_t(a.hc) * nk + nk);
+  int64_t pairs = max_resident_pairs();
+  if (pairs > items) pairs = items;
 
   FusedParams p{};
   p.q = a.q;
@@ -535,38 +772,36 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool /*pdl*/) {
   p.out = a.out;
   p.gate_out = a.gate_out;
   p.kv_out = a.kv_out;
-  p.gx = gx;
-  p.flags = flags;
+  p.gx = reinterpret_cast<float*>(base + l.gx);
+  p.part = reinterpret_cast<float*>(base + l.part);
+  p.next = sync;
+  p.count = sync + 1;
+  p.flags = sync + 1 + m_tiles * 2 * a.hc;
   p.M = a.M;
   p.K = a.K;
   p.hc = a.hc;
   p.dim = a.dim;
-  p.bnv = bnv;
-  p.m_tiles = static_cast<int32_t>(m_tiles);
   p.eps = a.eps;
   p.inv_sqrt_dim = a.inv_sqrt_dim;
   p.err = a.err;
   p.adv = a.adv;
+  p.sched = make_fused_schedule(m_tiles, a.hc * nk, nk, static_cast<int32_t>(pairs));
 
-  // persistent: slots of token tiles with hc pairs each, all resident together
-  int64_t slots = max_resident_pairs() / a.hc;
-  if (slots < 1) return cudaErrorNotSupported;
-  if (slots > m_tiles) slots = m_tiles;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(2, static_cast<unsigned>(a.hc), static_cast<unsigned>(slots));
+  cfg.gridDim = dim3(2, static_cast<unsigned>(pairs), 1);
   cfg.blockDim = dim3(kFusedThreads, 1, 1);
-  cfg.dynamicSmemBytes = fused_smem_bytes(a.dim);
+  cfg.dynamicSmemBytes = fused_smem_bytes();
   cfg.stream = st;
-  cudaLaunchAttribute attr[2];
+  // No co-residency is needed: a pair takes items only while it runs, and takes them in the
+  // schedule's order, so every item a value item waits for is held by a running pair.
+  cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeCooperative;   // the gate exchange needs co-residency
-  attr[1].val.cooperative = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, engram_fused_kernel, tmA, tmWk, tmWv, tmX, p);
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, engram_fused_kernel, tmA, tmW, tmX, tmOut, p);
 }
 
 }  // namespace engram

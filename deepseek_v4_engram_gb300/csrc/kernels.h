@@ -112,7 +112,7 @@ struct FusedArgs {
   float eps, inv_sqrt_dim;
   uint32_t* err;
   LenAdvance adv;         // adv.len may be null
-  void* scratch;          // fused_scratch_bytes(M, hc) bytes, 256-byte aligned
+  void* scratch;          // fused_scratch_bytes(M, hc, dim) bytes, 256-byte aligned
 };
 
 // `pdl`: launch with programmatic stream serialization (the kernel then overlaps its launch and
@@ -128,7 +128,7 @@ bool small_supported(int64_t M, int32_t N, int32_t K);
 int small_ksplit(int32_t N, int32_t K);
 cudaError_t launch_wkv_small(const WkvSmallArgs& a, cudaStream_t s, bool pdl = false);
 bool fused_supported(int32_t K, int32_t hc, int32_t dim);
-size_t fused_scratch_bytes(int64_t M, int32_t hc);
+size_t fused_scratch_bytes(int64_t M, int32_t hc, int32_t dim);
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s, bool pdl = false);
 
 // cudaLaunchKernelEx with optional programmatic stream serialization.

@@ -189,12 +189,15 @@ ENGRAM_API int engram_gate_and_add(const engram_desc_t* desc, const uint16_t* x,
  *   wkv bf16 [dim * (hc + 1), n_hash_cols * head_dim]; x, q_weight, k_weight, token_mask, out,
  *   gate_out as in engram_gate_and_add; kv_out bf16 [M, dim * (hc + 1)] or NULL;
  *   workspace: device scratch of at least engram_wkv_gate_workspace_size(desc, M) bytes,
- *   256-byte aligned, not shared with a concurrent call (the gates the streams exchange).
- * The kernel is a cooperative launch (all of its CTAs resident at once); a launch that cannot be
- * co-resident returns ENGRAM_ECUDA. Results equal engram_wkv followed by engram_gate_and_add up
- * to f32 summation order in the gate. Requires n_hash_cols * head_dim % 64 == 0, dim % 256 == 0,
- * dim <= 5120, hc_mult <= 8 and dim / hc_mult a multiple of 64; otherwise returns
- * ENGRAM_EUNSUPPORTED (use the two separate calls).
+ *   256-byte aligned, not shared with a concurrent call (per-column-tile partial sums of the
+ *   gate, the gates, and the counters and flags the CTAs coordinate through; the counters are
+ *   cleared on the stream before each launch, so nothing in it needs to start at zero).
+ * The kernel is persistent (one CTA per SM) but does not need all of its CTAs resident at once:
+ * CTAs take work in an order in which everything a CTA waits for is held by a running CTA.
+ * Results equal engram_wkv followed by engram_gate_and_add up
+ * to f32 summation order in the gate, and are the same from run to run. Requires
+ * n_hash_cols * head_dim % 64 == 0, dim % 256 == 0, dim <= 5120 and hc_mult <= 8; otherwise
+ * returns ENGRAM_EUNSUPPORTED (use the two separate calls).
  */
 ENGRAM_API size_t engram_wkv_gate_workspace_size(const engram_desc_t* desc, int64_t M);
 ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
@@ -206,9 +209,9 @@ ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
 /*
  * Bytes of scratch for engram_forward on M = B * T tokens with the fastest projection path (a
  * multiple of 256). engram_forward also accepts a smaller workspace and then runs the fastest
- * path that fits it; the smallest it accepts holds the gathered rows and the exchanged gates
- * (3,088 bytes per token at the full geometry, plus 32 bytes per 256 tokens, each part rounded
- * up to a multiple of 256).
+ * path that fits it; the smallest it accepts holds the gathered rows and the fused kernel's
+ * scratch (4,048 bytes per token at the full geometry, plus 64 bytes per 256 tokens and 4 bytes,
+ * each part rounded up to a multiple of 256).
  */
 ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64_t M);
 
@@ -223,8 +226,8 @@ ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64
  *   engram_forward_workspace_size for its size.
  * How stages 3 and 4 run depends on M and on the workspace given (the fastest path that fits):
  * up to 256 tokens, a weight-streaming projection over every SM (split-K partials for decode-
- * sized batches) then the gate kernel; below 4096 tokens, the persistent projection GEMM into
- * a bf16 kv then the gate kernel; from 4096 tokens, or when only the minimum workspace is given,
+ * sized batches) then the gate kernel; below 1024 tokens, the persistent projection GEMM into
+ * a bf16 kv then the gate kernel; from 1024 tokens, or when only the minimum workspace is given,
  * the projection with the gate fused into its epilogue (as engram_wkv_gate). Every path runs
  * on the GPU; results agree within the projection's f32-summation bound.
  */
@@ -246,7 +249,7 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
  * lives in a fixed array of ENGRAM_NOALLOC_SCRATCH_BYTES (8 MiB) that the library keeps in every
  * GPU that loads it, until the process exits. A call whose scratch would not fit returns
  * ENGRAM_EINVAL and launches nothing: at the full geometry (dim 5120, hc 4, 24 rows of
- * head_dim 64) that is more than 2,716 tokens (B * T) per call. Within that limit the call runs
+ * head_dim 64) that is more than 2,048 tokens (B * T) per call. Within that limit the call runs
  * the fastest projection path whose scratch fits in the array.
  *
  * This call allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. Its

@@ -49,11 +49,11 @@ def wide():
 
 def ws_for(dm, M, mode):
     """Workspace sized to select a path: "fastest" (the reported size), "kv" (room for a bf16 kv,
-    no split-K partials), or "min" (rows + the fused kernel's gate exchange: the fused kernel)."""
+    no split-K partials), or "min" (rows + the fused kernel's scratch: the fused kernel)."""
     g = dm.geom
     r = lambda n: (n + 255) // 256 * 256
     base = r(M * g.K * 2)
-    fused = eg.api.engram_wkv_gate_workspace_size(dm.desc, M)   # gates the streams exchange
+    fused = eg.api.engram_wkv_gate_workspace_size(dm.desc, M)   # partial sums, gates, counters
     n = {"fastest": eg.engram_forward_workspace_size(dm.desc, M), "kv": base + r(M * g.N * 2),
          "min": base + fused}[mode]
     return torch.empty(max(n, 256), dtype=torch.uint8, device="cuda")
