@@ -90,9 +90,11 @@ def kernel_traffic(kernel: str):
     try:
         with open(path) as f:
             d = json.load(f)[kernel]
-        src = os.path.join(ROOT, d["source"])
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
-        if sha != d["source_sha"]:
+        h = hashlib.sha256()
+        for src in d["sources"]:   # every file the kernel is compiled from, in order
+            with open(os.path.join(ROOT, src), "rb") as f:
+                h.update(f.read())
+        if h.hexdigest()[:16] != d["source_sha"]:
             return None
         return {"bytes_per_launch": d["bytes_per_launch"], "tokens_per_launch": d["tokens"]}
     except (OSError, KeyError, ValueError):
