@@ -144,19 +144,22 @@ HashArgs make_hash_args(const engram_desc_t* d, const engram_tables_t* t, const 
 constexpr size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
 // How engram_forward runs stages 3 and 4 for a given token count, fastest first:
+//  - kDecode:  M <= 64: weight-streaming projection in 64-row units, a fixed share per SM, into
+//              a bf16 kv (no partial sums), then the gate kernel;
 //  - kSmall:   M <= 256: weight-streaming projection over every SM (split-K partials in f32 when
 //              the workspace holds them, else bf16 kv), then the gate kernel;
 //  - kUnfused: the persistent projection GEMM into a bf16 kv, then the gate kernel; measured
 //              faster than the fused kernel below 1024 tokens (too few items to fill the GPU
 //              past the fused kernel's cold start);
 //  - kFused:   projection + gate in one kernel; kv never touches HBM; least workspace.
-enum class Path { kSmall, kUnfused, kFused };
+enum class Path { kDecode, kSmall, kUnfused, kFused };
 struct Plan {
   Path path;
   int ksplit;
   size_t bytes;
 };
 constexpr int64_t kFusedMinTokens = 1024;
+constexpr int kMaxPlans = 6;
 
 // Candidate plans in order of preference; returns how many were written.
 int forward_plans(const engram_desc_t* d, int64_t M, Plan* out) {
@@ -167,6 +170,7 @@ int forward_plans(const engram_desc_t* d, int64_t M, Plan* out) {
   const size_t kv_bytes = round256(size_t(M) * N * 2);
   const bool fused = fused_supported(K, d->hc_mult, d->dim);
   int n = 0;
+  if (decode_supported(M, N, K)) out[n++] = {Path::kDecode, 1, base + kv_bytes};
   if (small_supported(M, N, K)) {
     // split-K only while its f32 partial sums stay small (decode-sized batches)
     const int ks = M <= 64 ? small_ksplit(N, K) : 1;
@@ -230,7 +234,7 @@ bool tensor_map_2d_bf16(void* map_out, const void* base, uint64_t inner, uint64_
 // Smallest workspace engram_forward accepts for M tokens (0 for an invalid descriptor).
 size_t forward_min_workspace_bytes(const engram_desc_t* desc, int64_t M) {
   if (check_desc(desc) != ENGRAM_OK || M < 0) return 0;
-  Plan plans[5];
+  Plan plans[kMaxPlans];
   const int n = forward_plans(desc, M, plans);
   size_t best = 0;
   for (int i = 0; i < n; ++i)
@@ -336,7 +340,8 @@ ENGRAM_API int engram_wkv(const uint16_t* a, const uint16_t* w, uint16_t* kv, in
   cudaError_t e;
   uint32_t* err = error_word(&e);
   if (!err) return cuda_fail(e, "engram_wkv");
-  if (small_supported(M, N, K)) {   // few tokens: stream the weight over every SM
+  if (decode_supported(M, N, K) || small_supported(M, N, K)) {
+    // few tokens: stream the weight over every SM
     WkvSmallArgs g{};
     g.a = a;
     g.w = w;
@@ -346,8 +351,9 @@ ENGRAM_API int engram_wkv(const uint16_t* a, const uint16_t* w, uint16_t* kv, in
     g.K = K;
     g.ksplit = 1;
     g.err = err;
-    if ((e = launch_wkv_small(g, static_cast<cudaStream_t>(stream))) != cudaSuccess)
-      return cuda_fail(e, "engram_wkv");
+    e = decode_supported(M, N, K) ? launch_wkv_decode(g, static_cast<cudaStream_t>(stream))
+                                  : launch_wkv_small(g, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "engram_wkv");
     return ENGRAM_OK;
   }
   WkvArgs g{a, w, kv, M, N, K, err};
@@ -457,7 +463,7 @@ ENGRAM_API int engram_wkv_gate(const engram_desc_t* desc, const uint16_t* rows,
 
 ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64_t M) {
   if (check_desc(desc) != ENGRAM_OK || M < 0) return 0;
-  Plan plans[5];
+  Plan plans[kMaxPlans];
   const int n = forward_plans(desc, M, plans);
   return n > 0 ? plans[0].bytes : 0;
 }
@@ -488,7 +494,7 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
     return fail(ENGRAM_EUNSUPPORTED, "needs n_hash_cols * head_dim %% 64 == 0");
   if (kv_out && !aligned(kv_out, 16)) return fail(ENGRAM_EINVAL, "kv_out must be 16-byte aligned");
   // the fastest plan whose scratch fits the workspace
-  Plan plans[5];
+  Plan plans[kMaxPlans];
   const int nplans = forward_plans(desc, M, plans);
   const Plan* plan = nullptr;
   size_t min_bytes = ~size_t(0);
@@ -507,11 +513,6 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   uint16_t* rows = reinterpret_cast<uint16_t*>(ws);   // the projection's input [M, K]
-  ws += round256(size_t(M) * K * 2);
-
-  // 1+2. hash every slot and gather its row into the projection's input, in one kernel. The
-  // kernels of the chain are launched with programmatic stream serialization: each overlaps its
-  // launch and prologue with the previous one and waits for it before touching its data.
   HashArgs h = make_hash_args(desc, tables, tokens, B, T, cache, cache_len, capacity,
                               hash_ids_out, err);
   HashRowsArgs hr{};
@@ -521,12 +522,16 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   hr.num_rows = desc->num_embeddings;
   hr.head_dim = desc->head_dim;
   hr.rows = rows;
+  // the kernel that runs last advances the cache lengths (every reader of them is done)
+  const LenAdvance adv{cache_len, B, T, capacity};
+  const float inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));
+
+  // 1+2. hash every slot and gather its row into the projection's input, in one kernel. The
+  // kernels of the chain are launched with programmatic stream serialization: each overlaps its
+  // launch and prologue with the previous one and waits for it before touching its data.
+  ws += round256(size_t(M) * K * 2);
   if ((e = launch_hash_rows(hr, st, true)) != cudaSuccess)
     return cuda_fail(e, "engram_forward: hash + rows");
-  // the last kernel of the chain advances the cache lengths (every reader of them is done)
-  const LenAdvance adv{cache_len, B, T, capacity};
-
-  const float inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));
   if (plan->path == Path::kFused) {
     // 3+4. projection with the gate fused into its epilogue
     FusedArgs f = make_fused_args(desc, rows, wts->wkv, x, wts->q_weight, wts->k_weight,
@@ -538,7 +543,20 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   }
   // 3. projection -> bf16 kv (or f32 split-K partials); 4. gate and add
   GateArgs ga{};
-  if (plan->path == Path::kSmall) {
+  if (plan->path == Path::kDecode) {
+    WkvSmallArgs g{};
+    g.a = rows;
+    g.w = wts->wkv;
+    g.kv = kv_out ? kv_out : reinterpret_cast<uint16_t*>(ws);
+    g.M = M;
+    g.N = N;
+    g.K = K;
+    g.ksplit = 1;
+    g.err = err;
+    if ((e = launch_wkv_decode(g, st, true)) != cudaSuccess)
+      return cuda_fail(e, "engram_forward: wkv");
+    ga.kv = g.kv;
+  } else if (plan->path == Path::kSmall) {
     WkvSmallArgs g{};
     g.a = rows;
     g.w = wts->wkv;

@@ -326,6 +326,14 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
+// Prefetch a 2-D box into L2 (no shared memory, nothing to wait for).
+__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
+}
+
 // 3-D tiled store of a shared-memory box to global memory (rows past the tensor's end are not
 // written). Completion is tracked per thread with bulk async-groups.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int32_t x,
@@ -379,9 +387,17 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
-// Barrier `id` (1..15) among `nthreads` threads (a multiple of 32) of this CTA.
+// Barrier `id` (1..15) among `nthreads` threads (a multiple of 32) of this CTA. The non-aligned
+// form counts every thread on its own, so it is correct where the lanes of a warp arrive at
+// different times (after a branch that one lane took alone).
 __device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t nthreads) {
-  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+  asm volatile("barrier.sync %0, %1;" ::"r"(id), "r"(nthreads) : "memory");
+}
+
+// Barrier over every thread of the CTA, non-aligned (see named_bar_sync): for the teardown of the
+// warp-specialised kernels, whose warps reach it from different roles.
+__device__ __forceinline__ void cta_sync_all() {
+  asm volatile("barrier.sync 0;" ::: "memory");
 }
 
 // ----------------------------------------------------------------------------------- clusters

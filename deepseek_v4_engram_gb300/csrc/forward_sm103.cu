@@ -188,13 +188,13 @@ __device__ bool wait_flags(const int32_t* flags, int hc, volatile int* abort, ui
   return true;
 }
 
-// bar.red.or over the epilogue warps: a barrier that also tells every thread whether any of them
-// passed `pred`.
+// barrier.red.or over the epilogue warps (non-aligned: every thread counted on its own): a
+// barrier that also tells every thread whether any of them passed `pred`.
 __device__ __forceinline__ bool epi_any(bool pred) {
   uint32_t r;
   asm volatile(
       "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
-      "bar.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      "barrier.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
       : "=r"(r)
       : "r"(static_cast<uint32_t>(pred)), "r"(kEpiBarrier), "r"(kEpiThreads)
       : "memory");

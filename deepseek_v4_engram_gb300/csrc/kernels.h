@@ -127,6 +127,9 @@ cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t s, bool pdl = false);
 bool small_supported(int64_t M, int32_t N, int32_t K);
 int small_ksplit(int32_t N, int32_t K);
 cudaError_t launch_wkv_small(const WkvSmallArgs& a, cudaStream_t s, bool pdl = false);
+// Weight-streaming projection for M <= 64 tokens (decode): bf16 kv, no partial sums.
+bool decode_supported(int64_t M, int32_t N, int32_t K);
+cudaError_t launch_wkv_decode(const WkvSmallArgs& a, cudaStream_t s, bool pdl = false);
 bool fused_supported(int32_t K, int32_t hc, int32_t dim);
 size_t fused_scratch_bytes(int64_t M, int32_t hc, int32_t dim);
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s, bool pdl = false);

@@ -185,7 +185,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   }
 
   tc_fence_before();
-  __syncthreads();
+  __syncwarp();
+  cta_sync_all();   // every role is done with TMEM (each thread counted on its own)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, kTmemCols);
