@@ -169,7 +169,7 @@ def test_wkv_tiny_within_one_ulp(tiny, M):
     assert_kv_close(host(kv), E.linear_bf16(a, tiny.model.wkv), a, tiny.model.wkv)
 
 
-@pytest.mark.parametrize("M", [1, 200, 513])
+@pytest.mark.parametrize("M", [1, 33, 64, 200, 513])
 def test_wkv_full_width_within_one_ulp(wide, M):
     rng = np.random.default_rng(M + 1)
     ids = rng.integers(0, wide.model.tables.num_embeddings, (M, 24))
