@@ -530,6 +530,8 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   // kernels of the chain are launched with programmatic stream serialization: each overlaps its
   // launch and prologue with the previous one and waits for it before touching its data.
   ws += round256(size_t(M) * K * 2);
+  if (plan->path == Path::kFused)   // the fused kernel's counters, cleared by the hash kernel
+    fused_sync_region(ws, M, desc->hc_mult, desc->dim, &hr.zero, &hr.zero_n);
   if ((e = launch_hash_rows(hr, st, true)) != cudaSuccess)
     return cuda_fail(e, "engram_forward: hash + rows");
   if (plan->path == Path::kFused) {
@@ -538,6 +540,7 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
                                   token_mask, out, gate_out, kv_out, M, err);
     f.adv = adv;
     f.scratch = ws;
+    f.sync_cleared = true;
     if ((e = launch_fused(f, st, true)) != cudaSuccess) return cuda_fail(e, "engram_forward: fused");
     return ENGRAM_OK;
   }

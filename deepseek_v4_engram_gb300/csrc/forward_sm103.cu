@@ -737,7 +737,14 @@ size_t fused_scratch_bytes(int64_t M, int32_t hc, int32_t dim) {
   return scratch_layout(M, hc, dim).total;
 }
 
-cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool /*pdl*/) {
+void fused_sync_region(void* scratch, int64_t M, int32_t hc, int32_t dim, int32_t** ptr,
+                       int32_t* count) {
+  const ScratchLayout l = scratch_layout(M, hc, dim);
+  *ptr = reinterpret_cast<int32_t*>(static_cast<uint8_t*>(scratch) + l.sync);
+  *count = static_cast<int32_t>(l.sync_bytes / 4);
+}
+
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl) {
   const int64_t N = static_cast<int64_t>(a.dim) * (a.hc + 1);
   const int64_t m_tiles = (a.M + kTokensPerTile - 1) / kTokensPerTile;
   alignas(64) CUtensorMap tmA, tmW, tmX, tmOut;
@@ -757,8 +764,10 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool /*pdl*/) {
   const ScratchLayout l = scratch_layout(a.M, a.hc, a.dim);
   uint8_t* base = static_cast<uint8_t*>(a.scratch);
   int32_t* sync = reinterpret_cast<int32_t*>(base + l.sync);
-  cudaError_t e = cudaMemsetAsync(sync, 0, l.sync_bytes, st);
-  if (e != cudaSuccess) return e;
+  if (!a.sync_cleared) {
+    cudaError_t e = cudaMemsetAsync(sync, 0, l.sync_bytes, st);
+    if (e != cudaSuccess) return e;
+  }
 
   const int32_t nk = a.dim / kBN;
   const int64_t items = m_tiles * (int64_t(a.hc) * nk + nk);
@@ -794,13 +803,17 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool /*pdl*/) {
   cfg.stream = st;
   // No co-residency is needed: a pair takes items only while it runs, and takes them in the
   // schedule's order, so every item a value item waits for is held by a running pair.
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // with the counters already cleared by the previous kernel, the launch and prologue overlap
+  // it; the kernel waits for it before touching its data
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = (pdl && a.sync_cleared) ? 2 : 1;
   return cudaLaunchKernelEx(&cfg, engram_fused_kernel, tmA, tmW, tmX, tmOut, p);
 }
 

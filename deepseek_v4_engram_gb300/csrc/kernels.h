@@ -36,6 +36,8 @@ struct HashRowsArgs {
   int64_t num_rows;
   int32_t head_dim;
   uint16_t* rows;         // [B*T, S, hd] bf16
+  int32_t* zero;          // optional: zero_n int32 set to 0 (the next kernel's counters)
+  int32_t zero_n;
 };
 
 // Advance cache_len[b] += T (clamped to capacity) for b < B; done by one block of the last kernel
@@ -113,7 +115,12 @@ struct FusedArgs {
   uint32_t* err;
   LenAdvance adv;         // adv.len may be null
   void* scratch;          // fused_scratch_bytes(M, hc, dim) bytes, 256-byte aligned
+  bool sync_cleared;      // the scratch's counters were cleared by the previous kernel
 };
+
+// The counters in the fused kernel's scratch that must be zero when it starts.
+void fused_sync_region(void* scratch, int64_t M, int32_t hc, int32_t dim, int32_t** ptr,
+                       int32_t* count);
 
 // `pdl`: launch with programmatic stream serialization (the kernel then overlaps its launch and
 // prologue with the previous kernel of the stream and waits for it before touching its data).

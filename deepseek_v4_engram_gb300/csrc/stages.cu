@@ -110,6 +110,9 @@ constexpr int kHrThreads = 256;
 __global__ void __launch_bounds__(kHrThreads) hash_rows_kernel(HashRowsArgs a) {
   pdl_wait();
   pdl_launch_dependents();
+  // the next kernel's counters (it reads them only after this grid has completed)
+  if (a.zero != nullptr && blockIdx.x == 0)
+    for (int32_t i = threadIdx.x; i < a.zero_n; i += blockDim.x) a.zero[i] = 0;
   const HashArgs& h = a.hash;
   const int32_t S = (h.max_ngram - 1) * h.n_heads;
   const int64_t M = static_cast<int64_t>(h.B) * h.T;
