@@ -326,14 +326,6 @@ __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* m
       : "memory");
 }
 
-// Prefetch a 2-D box into L2 (no shared memory, nothing to wait for).
-__device__ __forceinline__ void tma_prefetch_2d(const CUtensorMap* map, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // 3-D tiled store of a shared-memory box to global memory (rows past the tensor's end are not
 // written). Completion is tracked per thread with bulk async-groups.
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void* src, int32_t x,
