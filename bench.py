@@ -48,6 +48,8 @@ def parse_args(argv=None):
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-decode", action="store_true")
+    p.add_argument("--no-configs", action="store_true",
+                   help="skip the masked batched prefill and the T sweep")
     return p.parse_args(argv)
 
 
@@ -279,6 +281,10 @@ def run_native(args):
     decode = None if args.no_decode else run_decode(eg, desc, tables, weights, model, geom, args,
                                                     flush, peaks)
 
+    configs = None
+    if not args.no_configs and world == 1:
+        configs = run_configs(eg, desc, tables, weights, model, geom, flush, peaks)
+
     e2e = None
     if not args.no_e2e:
         e2e = run_e2e(eg, desc, tables, weights, batch, geom, args, world)
@@ -301,6 +307,7 @@ def run_native(args):
         "step_roofline_frac": round(t_roof / step_s, 4),
         "gpu_launches": 2 * args.steps,
         "decode": decode,
+        "configs": configs,
         "clocks": clocks.summary(),
         "e2e": e2e,
         "cpu_baseline": cpu,
@@ -328,6 +335,92 @@ def capture_graph(fn):
         fn()
     torch.cuda.synchronize()
     return graph
+
+
+def time_forward(eg, desc, tables, weights, x, tokens, mask, B, T, flush, steps, warmup):
+    """Mean ms per step of engram_forward on B sequences of T new tokens: a captured graph
+    replayed per step, L2 flushed before each step (outside the events)."""
+    import torch
+    M = B * T
+    cache = torch.zeros((B, T * (steps + warmup + 2)), dtype=torch.int32, device="cuda")
+    cache_len = torch.zeros(B, dtype=torch.int32, device="cuda")
+    out = torch.empty_like(x)
+    ws = torch.empty(eg.engram_forward_workspace_size(desc, M), dtype=torch.uint8, device="cuda")
+
+    def step():
+        eg.engram_forward(desc, tables, weights, x, tokens, cache, cache_len, mask, out, ws)
+
+    graph = capture_graph(step)
+    for _ in range(warmup):
+        flush.zero_()
+        graph.replay()
+    ev = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    if eg.engram_check_errors() != 0:
+        raise RuntimeError("device error word set")
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def roofline_of(M, ms, peaks):
+    t_flop = FLOPS_PER_TOKEN * M / (peaks["bf16_tflops"] * 1e12)
+    t_byte = (M * BYTES_PER_TOKEN + WKV_BYTES) / (peaks["hbm_gbs"] * 1e9)
+    return ("tensor" if t_flop >= t_byte else "hbm"), max(t_flop, t_byte) / (ms / 1e3)
+
+
+def run_configs(eg, desc, tables, weights, model, geom, flush, peaks):
+    """The masked batched prefill (B8 T8192: pow2 block scales, Student-t x, ~10% of positions
+    masked in contiguous spans) and the T sweep at B1; each step through engram_forward."""
+    import numpy as np
+    import torch
+    import synth
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int16) if a.dtype == np.uint16 else a).cuda()
+
+    res = {}
+    w = synth.WORKLOADS["masked_b8_t8192"]
+    pm = synth.make_model(geom, w["model_seed"], scale_mode=w["scale_mode"])
+    pw = eg.DeviceWeights(dev(pm.table), dev(pm.scales), weights.wkv, weights.q_weight,
+                          weights.k_weight)
+    # tokens and mask from the host generators; x (2.7 GB) drawn on the device
+    rng = np.random.default_rng(w["batch_seed"])
+    tokens = synth.make_tokens(geom, w["B"], w["T"], rng)
+    mask = synth.make_span_mask(w["B"], w["T"], w["mask_frac"], rng)
+    x = synth.make_x_device((w["B"], w["T"], geom.hc_mult, geom.dim), w["batch_seed"],
+                            w["x_dist"])
+    M = w["B"] * w["T"]
+    ms = time_forward(eg, desc, tables, pw, x, dev(tokens), dev(mask.astype(np.uint8)), w["B"],
+                      w["T"], flush, steps=5, warmup=3)
+    bound, frac = roofline_of(M, ms, peaks)
+    res["masked"] = {"workload": "masked prefill B8 T8192 (pow2 scales, Student-t x, ~10% masked "
+                                 "spans)", "value": round(M / (ms / 1e3), 1), "unit": "tokens/s",
+                     "ms_per_step": round(ms, 4), "bound": bound, "roofline_frac": round(frac, 4)}
+    del pw, x
+    w = synth.WORKLOADS["sweep_b1"]
+    tmax = max(w["T_list"])
+    tok_all = dev(synth.make_tokens(geom, 1, tmax, np.random.default_rng(w["batch_seed"])))
+    x_all = synth.make_x_device((1, tmax, geom.hc_mult, geom.dim), w["batch_seed"])
+    sweep = []
+    for T in w["T_list"]:
+        steps = 20 if T <= 4096 else 5
+        ms = time_forward(eg, desc, tables, weights, x_all[:, :T].contiguous(),
+                          tok_all[:, :T].contiguous(), None, 1, T, flush, steps=steps, warmup=3)
+        bound, frac = roofline_of(T, ms, peaks)
+        sweep.append({"T": T, "value": round(T / (ms / 1e3), 1), "us_per_step": round(ms * 1e3, 2),
+                      "bound": bound, "roofline_frac": round(frac, 4)})
+    res["sweep"] = {"workload": "prefill B1, T = 1 .. 65536", "unit": "tokens/s",
+                    "points": sweep,
+                    "crossover_tokens": round(WKV_BYTES / (FLOPS_PER_TOKEN / (peaks["bf16_tflops"]
+                                              * 1e12) * peaks["hbm_gbs"] * 1e9 - BYTES_PER_TOKEN))}
+    return res
 
 
 def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64, prefill=2048):

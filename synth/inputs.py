@@ -171,6 +171,28 @@ def make_x(shape, rng: np.random.Generator, dist: str = "normal",
     return out.reshape(shape)
 
 
+def make_x_device(shape, seed: int, dist: str = "normal", device: str = "cuda"):
+    """Device-drawn x[..., hc, dim] as bf16 storage bits (torch int16), for benchmark batches too
+    large to draw on the host in reasonable time: the distributions of make_x (N(0,1), or
+    Student-t(nu=3)/sqrt(3) as a normal over sqrt(chi2_3 / 3)) from torch's generator seeded with
+    `seed`, with the same nudge of exact zeros. The numbers differ from make_x's; parity tests use
+    make_x."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    v = torch.randn(tuple(shape), generator=g, device=device, dtype=torch.float32)
+    if dist == "student_t3":
+        # chi2 with 3 degrees of freedom as a sum of three squared normals
+        c = torch.zeros_like(v)
+        for _ in range(3):
+            c.addcmul_(w := torch.randn(tuple(shape), generator=g, device=device), w)
+        v = v / torch.sqrt(c / 3.0) / math.sqrt(3.0)
+    elif dist != "normal":
+        raise ValueError(dist)
+    bits = v.to(torch.bfloat16).view(torch.int16)
+    zero = (bits & 0x7FFF) == 0
+    return torch.where(zero, (bits & -0x8000) | 0x0080, bits)
+
+
 def make_wkv(geom: Geometry, rng: np.random.Generator) -> np.ndarray:
     """wkv weight [N, K] bf16: U(-1,1) * K^-0.5 (fixture rule scale = in^-0.5)."""
     v = rng.uniform(-1.0, 1.0, size=(geom.N, geom.K)).astype(np.float32)
