@@ -32,7 +32,7 @@
 //   warps 2-9    epilogue: two warps per TMEM lane quadrant (warp w reads lanes 32*(w%4)...),
 //                thread = (token row, half of each 64-column box): tcgen05.ld, gate sums, output;
 //   warp 10      TMA producer of the residual streams x: 128-token x 64-column boxes into a
-//                3-slot ring, in exactly the order the epilogue consumes them;
+//                4-slot ring, in exactly the order the epilogue consumes them;
 //   warp 11      gate warp: counts each key tile in and, for the last one, forms and publishes the
 //                gates, off the epilogue's path.
 #include "device.cuh"
@@ -53,7 +53,7 @@ constexpr int kFusedStages = 5;            // A/B ring depth
 constexpr int kPairB = kBN / 2;            // wkv rows of a key tile staged by each CTA of a pair
 constexpr int kStageABytes = kBM * kBK * 2;
 constexpr int kStageBBytes = kPairB * kBK * 2;
-constexpr int kXSlots = 3;                 // x ring depth
+constexpr int kXSlots = 4;                 // x ring depth
 constexpr int kXCols = 64;                 // columns per x box (128 B per row: one swizzle row)
 constexpr int kXBoxBytes = kBM * kXCols * 2;
 constexpr int kItemSlots = 4;              // item ring depth
@@ -80,13 +80,16 @@ struct FusedShared {
   int32_t item[kItemSlots];       // item index, or -1: no more items
   uint32_t tmem_base;
   int abort;
-  float part[2][3][kBM];          // second-half partial sums, handed to the first half
+  // second-half partial sums, handed to the first half; one buffer suffices because the epilogue
+  // warps meet at a barrier after the first half has read it and before the next key tile
+  float part[3][kBM];
 };
 
-size_t fused_smem_bytes() {
-  return size_t(kFusedStages) * (kStageABytes + kStageBBytes) + size_t(kXSlots) * kXBoxBytes +
-         sizeof(FusedShared) + 1024;
-}
+constexpr size_t kFusedSmemBytes = size_t(kFusedStages) * (kStageABytes + kStageBBytes) +
+                                   size_t(kXSlots) * kXBoxBytes + sizeof(FusedShared) + 1024;
+static_assert(kFusedSmemBytes <= 232448, "fused kernel exceeds 227 KB of shared memory");
+
+size_t fused_smem_bytes() { return kFusedSmemBytes; }
 
 struct FusedParams {
   const uint16_t* q;
@@ -652,17 +655,17 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         const uint32_t b = nkey & 1, ph = (nkey >> 1) & 1;
         ++nkey;
         if (half == 1) {
-          sh->part[b][0][row] = sh2[0] + sh2[1];
-          sh->part[b][1][row] = sk2[0] + sk2[1];
-          sh->part[b][2][row] = shwk[0] + shwk[1];
+          sh->part[0][row] = sh2[0] + sh2[1];
+          sh->part[1][row] = sk2[0] + sk2[1];
+          sh->part[2][row] = shwk[0] + shwk[1];
         }
         if (epi_any(!ok)) break;
         if (half == 0) {
           const int64_t ts = (static_cast<int64_t>(it.mt) * 2 + half_m) * hc + s;
           float* pj = p.part + (ts * nk + it.col % nk) * 3 * kBM;
-          __stcg(pj + row, sh2[0] + sh2[1] + sh->part[b][0][row]);
-          __stcg(pj + kBM + row, sk2[0] + sk2[1] + sh->part[b][1][row]);
-          __stcg(pj + 2 * kBM + row, shwk[0] + shwk[1] + sh->part[b][2][row]);
+          __stcg(pj + row, sh2[0] + sh2[1] + sh->part[0][row]);
+          __stcg(pj + kBM + row, sk2[0] + sk2[1] + sh->part[1][row]);
+          __stcg(pj + 2 * kBM + row, shwk[0] + shwk[1] + sh->part[2][row]);
           ok = mbar_wait(&sh->pempty[b], ph ^ 1u, abort, p.err);
           ok = __all_sync(0xFFFFFFFFu, ok);
           if (ok) mbar_arrive(&sh->pfull[b]);
