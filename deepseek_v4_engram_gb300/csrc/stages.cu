@@ -119,6 +119,15 @@ __global__ void __launch_bounds__(kHrThreads) hash_rows_kernel(HashRowsArgs a) {
   const int64_t pos0 = static_cast<int64_t>(blockIdx.x) * kHrPositions;
   __shared__ int32_t cwin[kHrPositions][kHrMaxNgram];
 
+  // The multipliers and this thread's first slot constants are fetched now, so that their loads
+  // overlap phase 1's instead of adding a round trip to memory after it.
+  uint64_t mult[kHrMaxNgram];
+#pragma unroll
+  for (int k = 0; k < kHrMaxNgram; ++k) mult[k] = k < h.max_ngram ? __ldg(h.multipliers + k) : 0;
+  const int32_t s_first = threadIdx.x % S;
+  const uint64_t prime_first = __ldg(h.primes + s_first);
+  const int64_t offset_first = __ldg(h.offsets + s_first);
+
   // phase 1: the window c_{p-k} of every position of the block
   if (threadIdx.x < kHrPositions * h.max_ngram) {
     const int j = threadIdx.x / h.max_ngram, k = threadIdx.x % h.max_ngram;
@@ -147,10 +156,13 @@ __global__ void __launch_bounds__(kHrThreads) hash_rows_kernel(HashRowsArgs a) {
     if (bt >= M) break;
     const int32_t n = s / h.n_heads + 2;
     uint64_t mix = 0;
-    for (int32_t k = 0; k < n; ++k)
-      mix ^= static_cast<uint64_t>(static_cast<int64_t>(cwin[j][k])) * __ldg(h.multipliers + k);
-    const int32_t id =
-        static_cast<int32_t>(static_cast<int64_t>(mix % __ldg(h.primes + s)) + __ldg(h.offsets + s));
+#pragma unroll
+    for (int32_t k = 0; k < kHrMaxNgram; ++k)
+      if (k < n) mix ^= static_cast<uint64_t>(static_cast<int64_t>(cwin[j][k])) * mult[k];
+    const bool first = item == static_cast<int>(threadIdx.x);
+    const uint64_t prime = first ? prime_first : __ldg(h.primes + s);
+    const int64_t offset = first ? offset_first : __ldg(h.offsets + s);
+    const int32_t id = static_cast<int32_t>(static_cast<int64_t>(mix % prime) + offset);
     const int64_t i = bt * S + s;
     if (h.hash_ids) h.hash_ids[i] = id;
     uint4* dst = reinterpret_cast<uint4*>(a.rows + i * a.head_dim);
@@ -307,9 +319,6 @@ __device__ __forceinline__ float block_gate(const GateArgs& a, int64_t m, int32_
 // are issued before the reduction; kVec == 0: any dim, two passes over x.
 template <int kVec>
 __global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
-  pdl_wait();
-  pdl_launch_dependents();
-  advance_lengths(a.adv);
   const int64_t m = blockIdx.x / a.hc;
   const int32_t s = blockIdx.x % a.hc;
   const int64_t N = static_cast<int64_t>(a.dim) * (a.hc + 1);
@@ -325,17 +334,29 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
   float sh2 = 0.f, sk2 = 0.f, shwk = 0.f;
 
   if constexpr (kVec > 0) {
-    uint4 xv[kVec], vv[kVec];
+    // x, q, k and the mask are inputs of the forward that no kernel of its chain writes: they are
+    // loaded before waiting for the projection (the kernel ahead of this one in the stream)
+    uint4 xv[kVec], qv[kVec], kw[kVec], vv[kVec];
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
       const int v = threadIdx.x + j * kGateThreads;
       if (v < nvec) {
         xv[j] = __ldg(reinterpret_cast<const uint4*>(xr) + v);
+        qv[j] = __ldg(reinterpret_cast<const uint4*>(qr) + v);
+        kw[j] = __ldg(reinterpret_cast<const uint4*>(kr) + v);
+      }
+    }
+    pdl_wait();
+    pdl_launch_dependents();
+    advance_lengths(a.adv);
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const int v = threadIdx.x + j * kGateThreads;
+      if (v < nvec) {
         const uint4 kv = load_kv8(a, m, N, key0 + 8 * v);
         if (a.kv_out) reinterpret_cast<uint4*>(a.kv_out + m * N + key0)[v] = kv;
         if (keep || write_value) vv[j] = load_kv8(a, m, N, val0 + 8 * v);
-        acc_sums(xv[j], kv, __ldg(reinterpret_cast<const uint4*>(qr) + v),
-                 __ldg(reinterpret_cast<const uint4*>(kr) + v), sh2, sk2, shwk);
+        acc_sums(xv[j], kv, qv[j], kw[j], sh2, sk2, shwk);
       }
     }
     const float g = block_gate(a, m, s, sh2, sk2, shwk);
@@ -349,6 +370,9 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
       }
     }
   } else {
+    pdl_wait();
+    pdl_launch_dependents();
+    advance_lengths(a.adv);
     for (int v = threadIdx.x; v < nvec; v += kGateThreads) {
       const uint4 kv = load_kv8(a, m, N, key0 + 8 * v);
       if (a.kv_out) reinterpret_cast<uint4*>(a.kv_out + m * N + key0)[v] = kv;
