@@ -67,25 +67,47 @@ class NgramHashState:
 
     def push(self, tokens: np.ndarray) -> np.ndarray:
         """Append tokens [B, T] to the caches; return hash ids [B, T, n_hash_cols] (int64)."""
+        return self.push_layers(tokens, [(self.multipliers, self.primes, self.offsets)])[0]
+
+    def push_layers(self, tokens: np.ndarray, layers) -> list:
+        """Append tokens [B, T] to the caches once; return the hash ids of several Engram layers.
+
+        ``layers`` holds one (multipliers, primes, offsets) per layer. Each Engram layer takes its
+        own entry of the hash layout ([listing] __init__: layer_hash_index is the layer's place
+        in layout.layer_ids, and its embedding has that entry's num_embeddings rows), so each
+        layer has its own constants. Reading: the compressed token map and the cache of
+        compressed ids depend only on the tokens, so one cache serves every layer; each layer's
+        ids are formed from the same windows with its own constants. Returns a list with one
+        int64 array [B, T, n_hash_cols] per layer.
+        """
         tokens = np.asarray(tokens)
         B, T = tokens.shape
-        out = np.empty((B, T, self.n_hash_cols), dtype=np.int64)
+        outs = [np.empty((B, T, self.n_hash_cols), dtype=np.int64) for _ in layers]
         for b in range(B):
             p0 = len(self.cache[b])
             hist = np.concatenate([self.cache[b], self.token_map[tokens[b]]])   # step 1
             self.cache[b] = hist
             pos = p0 + np.arange(T)
-            mix = np.zeros(T, dtype=np.uint64)
-            for n in range(1, self.max_ngram_size + 1):
-                k = n - 1                                       # look-back of the new window cell
-                q = pos - k
-                c = np.where(q >= 0, hist[np.maximum(q, 0)], self.pad_id)      # step 2
-                mix = mix ^ (c.astype(np.uint64) * self.multipliers[k])        # steps 3-4
-                if n < 2:
-                    continue
-                for head in range(self.n_heads):                                # step 5
-                    s = (n - 2) * self.n_heads + head
-                    out[b, :, s] = (mix % self.primes[s]).astype(np.int64) + self.offsets[s]
+            for out, (multipliers, primes, offsets) in zip(outs, layers):
+                out[b] = self._slot_ids(hist, pos, np.asarray(multipliers, dtype=np.uint64),
+                                        np.asarray(primes, dtype=np.uint64),
+                                        np.asarray(offsets, dtype=np.int64))
+        return outs
+
+    def _slot_ids(self, hist, pos, multipliers, primes, offsets) -> np.ndarray:
+        """Steps 2-5 for the positions ``pos`` of one sequence whose compressed ids are ``hist``."""
+        out = np.empty((len(pos), self.n_hash_cols), dtype=np.int64)
+        mix = np.zeros(len(pos), dtype=np.uint64)
+        for n in range(1, self.max_ngram_size + 1):
+            k = n - 1                                       # look-back of the new window cell
+            q = pos - k
+            c = np.where(q >= 0, hist[np.maximum(q, 0)], self.pad_id)      # step 2
+            mix = mix ^ (c.astype(np.uint64) * multipliers[k])             # steps 3-4
+            if n < 2:
+                continue
+            for head in range(self.n_heads):                                # step 5
+                s = (n - 2) * self.n_heads + head
+                out[:, s] = (mix % primes[s]).astype(np.int64) + offsets[s]
         return out
 
 

@@ -107,6 +107,63 @@ def make_tables(geom: Geometry, rng: np.random.Generator, pad_id: int = 0) -> Ta
                   primes=primes, offsets=offsets)
 
 
+@dataclasses.dataclass
+class LayerHash:
+    """One Engram layer's own hash constants and fp8 table, for calls that serve several layers.
+
+    Each layer has its own entry of the hash layout (its own multipliers, primes, offsets and so
+    its own number of table rows); the token map and pad id are shared (they live in Tables).
+    table / scales are None when the caller draws them on the device instead.
+    """
+
+    multipliers: np.ndarray  # uint64 [max_ngram_size]
+    primes: np.ndarray       # uint64 [n_hash_cols]
+    offsets: np.ndarray      # int64 [n_hash_cols]
+    table: np.ndarray | None
+    scales: np.ndarray | None
+
+    @property
+    def num_embeddings(self) -> int:
+        return int(self.offsets[-1]) + int(self.primes[-1])
+
+
+def make_layer_hashes(geom: Geometry, n_layers: int, seed: int, prime_floor: int | None = None,
+                      scale_mode: str = "pow2", with_tables: bool = True) -> list:
+    """n_layers layers' hash constants (odd 64-bit multipliers; consecutive primes from a floor
+    that grows by 1/8 per layer, so every layer's table has its own size; cumulative offsets) and,
+    with_tables, their fp8 tables and e8m0 scales."""
+    rng = np.random.default_rng(seed)
+    floor = geom.prime_floor if prime_floor is None else prime_floor
+    out = []
+    for layer in range(n_layers):
+        multipliers = rng.integers(0, np.iinfo(np.uint64).max, size=geom.max_ngram_size,
+                                   dtype=np.uint64, endpoint=True) | np.uint64(1)
+        primes = np.array(consecutive_primes(floor + layer * (floor // 8), geom.n_hash_cols),
+                          dtype=np.uint64)
+        offsets = np.zeros(geom.n_hash_cols, dtype=np.int64)
+        offsets[1:] = np.cumsum(primes[:-1].astype(np.int64))
+        rows = int(offsets[-1]) + int(primes[-1])
+        table = make_fp8_rows(rows, geom.head_dim, rng) if with_tables else None
+        scales = make_scales(rows, geom.head_dim, rng, scale_mode) if with_tables else None
+        out.append(LayerHash(multipliers=multipliers, primes=primes, offsets=offsets,
+                             table=table, scales=scales))
+    return out
+
+
+def make_fp8_rows_device(num_rows: int, head_dim: int, seed: int, device: str = "cuda"):
+    """fp8 e4m3 codes [num_rows, head_dim] drawn on the device (torch generator): N(0,1) clamped
+    to +-448, cast by torch. For workloads too large to draw on the host in time."""
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    out = torch.empty((num_rows, head_dim), dtype=torch.uint8, device=device)
+    step = 1 << 22
+    for r0 in range(0, num_rows, step):
+        r1 = min(num_rows, r0 + step)
+        v = torch.randn((r1 - r0, head_dim), generator=g, device=device).clamp_(-448.0, 448.0)
+        out[r0:r1] = v.to(torch.float8_e4m3fn).view(torch.uint8)
+    return out
+
+
 def f32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
     """bf16 storage bits of a float32 array (torch's round-to-nearest-even cast)."""
     t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16)
