@@ -39,6 +39,15 @@ class EngramWeights(ctypes.Structure):
                 ("k_weight", ctypes.c_void_p)]
 
 
+class EngramLayerHash(ctypes.Structure):
+    _fields_ = [("multipliers", ctypes.c_void_p), ("primes", ctypes.c_void_p),
+                ("offsets", ctypes.c_void_p), ("num_embeddings", ctypes.c_int64),
+                ("table", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("rows", ctypes.c_void_p), ("hash_ids", ctypes.c_void_p)]
+
+
+MAX_HASH_LAYERS = 16
+
 _P = ctypes.c_void_p
 _I32 = ctypes.c_int32
 _I64 = ctypes.c_int64
@@ -53,6 +62,8 @@ SIGNATURES = {
     "engram_abi_version": (_I32, []),
     "engram_check_errors": (ctypes.c_int, [_P, ctypes.POINTER(ctypes.c_uint32)]),
     "engram_hash": (ctypes.c_int, [_DESC, _TAB, _P, _I32, _I32, _P, _P, _I32, _P, _P]),
+    "engram_hash_rows_layers": (ctypes.c_int, [_DESC, _TAB, ctypes.POINTER(EngramLayerHash), _I32,
+                                               _P, _I32, _I32, _P, _P, _I32, _P]),
     "engram_embed_rows": (ctypes.c_int, [_DESC, _P, _P, _P, _I64, _P, _P]),
     "engram_wkv": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P]),
     "engram_gate_and_add": (ctypes.c_int, [_DESC, _P, _P, _P, _P, _P, _P, _P, _I64, _P]),

@@ -12,7 +12,7 @@ from dataclasses import dataclass, field
 import torch
 
 from . import _lib
-from ._lib import EngramDesc, EngramTables, EngramWeights
+from ._lib import EngramDesc, EngramLayerHash, EngramTables, EngramWeights
 
 
 class EngramError(RuntimeError):
@@ -110,6 +110,39 @@ def engram_hash(desc, tables: DeviceTables, tokens, cache, cache_len, hash_ids, 
                              _ptr(tokens, "i32", "tokens"), B, T, _ptr(cache, "i32", "cache"),
                              _ptr(cache_len, "i32", "cache_len"), cache.shape[1],
                              _ptr(hash_ids, "i32", "hash_ids"), _stream(stream)))
+
+
+@dataclass
+class DeviceLayerHash:
+    """One Engram layer's hash constants, table and outputs for engram_hash_rows_layers."""
+
+    multipliers: torch.Tensor
+    primes: torch.Tensor
+    offsets: torch.Tensor
+    table: torch.Tensor
+    scales: torch.Tensor
+    rows: torch.Tensor
+    hash_ids: torch.Tensor | None = None
+    c: EngramLayerHash = field(init=False)
+
+    def __post_init__(self):
+        self.c = EngramLayerHash(_ptr(self.multipliers, "u64", "multipliers"),
+                                 _ptr(self.primes, "u64", "primes"),
+                                 _ptr(self.offsets, "i64", "offsets"), self.table.shape[0],
+                                 _ptr(self.table, "u8", "table"), _ptr(self.scales, "u8", "scales"),
+                                 _ptr(self.rows, "bf16", "rows"),
+                                 _ptr(self.hash_ids, "i32", "hash_ids"))
+
+
+def engram_hash_rows_layers(desc, tables: DeviceTables, layers, tokens, cache, cache_len,
+                            stream=None):
+    """Stages 1 + 2 for several layers (a list of DeviceLayerHash) in one launch."""
+    B, T = tokens.shape
+    arr = (EngramLayerHash * max(len(layers), 1))(*[lh.c for lh in layers])
+    _check(lib().engram_hash_rows_layers(
+        ctypes.byref(desc), ctypes.byref(tables.c), arr, len(layers),
+        _ptr(tokens, "i32", "tokens"), B, T, _ptr(cache, "i32", "cache"),
+        _ptr(cache_len, "i32", "cache_len"), cache.shape[1], _stream(stream)))
 
 
 def engram_embed_rows(desc, table, scales, ids, out, stream=None):

@@ -295,6 +295,70 @@ ENGRAM_API int engram_hash(const engram_desc_t* desc, const engram_tables_t* tab
   return ENGRAM_OK;
 }
 
+ENGRAM_API int engram_hash_rows_layers(const engram_desc_t* desc, const engram_tables_t* tables,
+                                       const engram_layer_hash_t* layers, int32_t n_layers,
+                                       const int32_t* tokens, int32_t B, int32_t T,
+                                       int32_t* cache, int32_t* cache_len, int32_t capacity,
+                                       void* stream) {
+  g_msg[0] = 0;
+  if (desc == nullptr || tables == nullptr) return fail(ENGRAM_EINVAL, "desc or tables is NULL");
+  if (layers == nullptr || n_layers < 1 || n_layers > ENGRAM_MAX_HASH_LAYERS)
+    return fail(ENGRAM_EINVAL, "layers must hold 1 to %d layer records", ENGRAM_MAX_HASH_LAYERS);
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const engram_layer_hash_t& L = layers[l];
+    if (!L.multipliers || !L.primes || !L.offsets || !L.table || !L.scales)
+      return fail(ENGRAM_EINVAL, "layer %d: a NULL pointer", l);
+    if (!aligned(L.multipliers, 8) || !aligned(L.primes, 8) || !aligned(L.offsets, 8) ||
+        !aligned(L.table, 16) || !aligned(L.rows, 16) || !aligned(L.hash_ids, 4))
+      return fail(ENGRAM_EINVAL, "layer %d: a misaligned pointer", l);
+    if (L.num_embeddings <= 0 || L.num_embeddings >= (int64_t(1) << 31))
+      return fail(ENGRAM_EINVAL, "layer %d: num_embeddings must be in [1, 2^31)", l);
+  }
+  // the checks of engram_hash, with layer 0's constants standing in for the tables' own
+  engram_desc_t d = *desc;
+  d.num_embeddings = layers[0].num_embeddings;
+  engram_tables_t t = *tables;
+  t.multipliers = layers[0].multipliers;
+  t.primes = layers[0].primes;
+  t.offsets = layers[0].offsets;
+  int rc = hash_checks(&d, &t, tokens, B, T, cache, cache_len, capacity, nullptr,
+                       /*ids_optional=*/true);
+  if (rc) return rc;
+  const int64_t M = int64_t(B) * T;
+  if (M == 0) return ENGRAM_OK;
+  if (M >= (int64_t(1) << 31)) return fail(ENGRAM_EINVAL, "B * T too large");
+  const int S = n_hash_cols(&d);
+  const size_t cache_bytes = size_t(B) * capacity * 4;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const engram_layer_hash_t& L = layers[l];
+    if (L.rows == nullptr) return fail(ENGRAM_EINVAL, "layer %d: rows is NULL", l);
+    const size_t row_bytes = size_t(M) * S * d.head_dim * 2, id_bytes = size_t(M) * S * 4;
+    if (overlaps(L.rows, row_bytes, cache, cache_bytes) ||
+        overlaps(L.rows, row_bytes, cache_len, size_t(B) * 4) ||
+        (L.hash_ids && (overlaps(L.hash_ids, id_bytes, cache, cache_bytes) ||
+                        overlaps(L.hash_ids, id_bytes, cache_len, size_t(B) * 4))))
+      return fail(ENGRAM_EINVAL, "layer %d: an output overlaps the cache", l);
+  }
+  cudaError_t e;
+  uint32_t* err = error_word(&e);
+  if (!err) return cuda_fail(e, "engram_hash_rows_layers");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  HashRowsArgs a{};
+  a.hash = make_hash_args(&d, &t, tokens, B, T, cache, cache_len, capacity, nullptr, err);
+  a.n_layers = n_layers;
+  a.head_dim = d.head_dim;
+  for (int32_t l = 0; l < n_layers; ++l) {
+    const engram_layer_hash_t& L = layers[l];
+    a.layer[l] = HashLayer{L.multipliers, L.primes,         L.offsets, L.table,
+                           L.scales,      L.num_embeddings, L.rows,    L.hash_ids};
+  }
+  if ((e = launch_hash_rows(a, st, true)) != cudaSuccess)
+    return cuda_fail(e, "engram_hash_rows_layers: hash + rows");
+  if ((e = launch_advance_len(cache_len, B, T, capacity, st)) != cudaSuccess)
+    return cuda_fail(e, "engram_hash_rows_layers: length update");
+  return ENGRAM_OK;
+}
+
 ENGRAM_API int engram_embed_rows(const engram_desc_t* desc, const uint8_t* table,
                                  const uint8_t* scales, const int32_t* ids, int64_t n_ids,
                                  uint16_t* out, void* stream) {
@@ -515,13 +579,8 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   uint16_t* rows = reinterpret_cast<uint16_t*>(ws);   // the projection's input [M, K]
   HashArgs h = make_hash_args(desc, tables, tokens, B, T, cache, cache_len, capacity,
                               hash_ids_out, err);
-  HashRowsArgs hr{};
-  hr.hash = h;
-  hr.table = wts->table;
-  hr.scales = wts->scales;
-  hr.num_rows = desc->num_embeddings;
-  hr.head_dim = desc->head_dim;
-  hr.rows = rows;
+  HashRowsArgs hr = single_layer_hash_rows(h, wts->table, wts->scales, desc->num_embeddings,
+                                           desc->head_dim, rows);
   // the kernel that runs last advances the cache lengths (every reader of them is done)
   const LenAdvance adv{cache_len, B, T, capacity};
   const float inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));

@@ -28,17 +28,37 @@ struct HashArgs {
   uint32_t* err;
 };
 
-// Stages 1 + 2 in one kernel: hash a position's slot and gather + dequantise its table row.
-struct HashRowsArgs {
-  HashArgs hash;          // hash.hash_ids may be null (ids then stay in registers)
-  const uint8_t* table;   // [rows, hd] e4m3
-  const uint8_t* scales;  // [rows, hd/32] e8m0
+// One Engram layer's share of the hash + gather kernel: its own hash constants and table.
+struct HashLayer {
+  const uint64_t* multipliers;  // [max_ngram]
+  const uint64_t* primes;       // [S]
+  const int64_t* offsets;       // [S]
+  const uint8_t* table;         // [num_rows, hd] e4m3
+  const uint8_t* scales;        // [num_rows, hd/32] e8m0
   int64_t num_rows;
+  uint16_t* rows;               // [B*T, S, hd] bf16
+  int32_t* hash_ids;            // [B*T, S] or null (ids then stay in registers)
+};
+
+constexpr int kMaxHashLayers = ENGRAM_MAX_HASH_LAYERS;
+
+// Stages 1 + 2 in one kernel for n_layers layers: the window of each position (token map, cache,
+// pad) is resolved once, then every layer hashes it with its own constants and gathers +
+// dequantises its own rows. hash.multipliers / primes / offsets / hash_ids are not read (each
+// layer's are in `layer`).
+struct HashRowsArgs {
+  HashArgs hash;
+  int32_t n_layers;
   int32_t head_dim;
-  uint16_t* rows;         // [B*T, S, hd] bf16
+  HashLayer layer[kMaxHashLayers];
   int32_t* zero;          // optional: zero_n int32 set to 0 (the next kernel's counters)
   int32_t zero_n;
 };
+
+// The single-layer form: layer 0 takes the constants and ids of `h` and the given table.
+HashRowsArgs single_layer_hash_rows(const HashArgs& h, const uint8_t* table,
+                                    const uint8_t* scales, int64_t num_rows, int32_t head_dim,
+                                    uint16_t* rows);
 
 // Advance cache_len[b] += T (clamped to capacity) for b < B; done by one block of the last kernel
 // of the forward, once every reader of the old lengths has finished.

@@ -98,16 +98,25 @@ __global__ void __launch_bounds__(256) rows_kernel(RowsArgs a) {
   }
 }
 
-// Stages 1 + 2 in one kernel, so the ids never make a round trip through memory. A block takes
-// kHrPositions consecutive positions: first one thread per (position, look-back k) resolves the
-// compressed id c_{p-k} (token map, cache or pad) into shared memory and appends c_p to the
-// cache; then one thread per (position, slot) forms the slot's mix and id from shared memory and
-// gathers + dequantises its table row (independent 16-byte loads).
-constexpr int kHrPositions = 8;
+// Stages 1 + 2 in one kernel, so the ids never make a round trip through memory, for one or
+// several Engram layers (each with its own hash constants and table: Engram listing, __init__,
+// layer_hash_index). A block takes `positions` consecutive positions: first one thread per
+// (position, look-back k) resolves the compressed id c_{p-k} (token map, cache or pad) into
+// shared memory once for all layers and appends c_p to the cache; then one thread per
+// (position, layer, slot) forms the slot's mix and id from shared memory and gathers +
+// dequantises its table row (independent 16-byte loads). `positions` is chosen so that a block's
+// (position, layer, slot) items fit its threads, so all of their row loads are in flight at once.
+constexpr int kHrMaxPositions = 8;
 constexpr int kHrMaxNgram = 8;
 constexpr int kHrThreads = 256;
 
-__global__ void __launch_bounds__(kHrThreads) hash_rows_kernel(HashRowsArgs a) {
+__host__ __device__ inline int32_t hash_rows_positions(int32_t items_per_position) {
+  const int32_t p = kHrThreads / items_per_position;
+  return p < 1 ? 1 : (p > kHrMaxPositions ? kHrMaxPositions : p);
+}
+
+__global__ void __launch_bounds__(kHrThreads)
+    hash_rows_kernel(const __grid_constant__ HashRowsArgs a) {
   pdl_wait();
   pdl_launch_dependents();
   // the next kernel's counters (it reads them only after this grid has completed)
@@ -115,21 +124,25 @@ __global__ void __launch_bounds__(kHrThreads) hash_rows_kernel(HashRowsArgs a) {
     for (int32_t i = threadIdx.x; i < a.zero_n; i += blockDim.x) a.zero[i] = 0;
   const HashArgs& h = a.hash;
   const int32_t S = (h.max_ngram - 1) * h.n_heads;
+  const int32_t LS = a.n_layers * S;   // items per position
+  const int32_t P = hash_rows_positions(LS);
   const int64_t M = static_cast<int64_t>(h.B) * h.T;
-  const int64_t pos0 = static_cast<int64_t>(blockIdx.x) * kHrPositions;
-  __shared__ int32_t cwin[kHrPositions][kHrMaxNgram];
+  const int64_t pos0 = static_cast<int64_t>(blockIdx.x) * P;
+  __shared__ int32_t cwin[kHrMaxPositions][kHrMaxNgram];
 
-  // The multipliers and this thread's first slot constants are fetched now, so that their loads
-  // overlap phase 1's instead of adding a round trip to memory after it.
+  // The constants of this thread's first item (its layer's multipliers, its slot's prime and
+  // offset) are fetched now, so that their loads overlap phase 1's instead of adding a round trip
+  // to memory after it.
+  const int32_t r_first = static_cast<int32_t>(threadIdx.x) % LS;
+  const HashLayer& lf = a.layer[r_first / S];
   uint64_t mult[kHrMaxNgram];
 #pragma unroll
-  for (int k = 0; k < kHrMaxNgram; ++k) mult[k] = k < h.max_ngram ? __ldg(h.multipliers + k) : 0;
-  const int32_t s_first = threadIdx.x % S;
-  const uint64_t prime_first = __ldg(h.primes + s_first);
-  const int64_t offset_first = __ldg(h.offsets + s_first);
+  for (int k = 0; k < kHrMaxNgram; ++k) mult[k] = k < h.max_ngram ? __ldg(lf.multipliers + k) : 0;
+  const uint64_t prime_first = __ldg(lf.primes + r_first % S);
+  const int64_t offset_first = __ldg(lf.offsets + r_first % S);
 
   // phase 1: the window c_{p-k} of every position of the block
-  if (threadIdx.x < kHrPositions * h.max_ngram) {
+  if (threadIdx.x < P * h.max_ngram) {
     const int j = threadIdx.x / h.max_ngram, k = threadIdx.x % h.max_ngram;
     const int64_t bt = pos0 + j;
     if (bt < M) {
@@ -148,32 +161,36 @@ __global__ void __launch_bounds__(kHrThreads) hash_rows_kernel(HashRowsArgs a) {
   }
   __syncthreads();
 
-  // phase 2: slot ids and rows
+  // phase 2: slot ids and rows, item = (position j, layer l, slot s)
   const int32_t chunks = a.head_dim / 16;
-  for (int item = threadIdx.x; item < kHrPositions * S; item += kHrThreads) {
-    const int j = item / S, s = item % S;
+  for (int item = threadIdx.x; item < P * LS; item += kHrThreads) {
+    const int j = item / LS, r = item % LS;
+    const int l = r / S, s = r % S;
     const int64_t bt = pos0 + j;
     if (bt >= M) break;
+    const HashLayer& L = a.layer[l];
+    const bool first = item == static_cast<int>(threadIdx.x);
     const int32_t n = s / h.n_heads + 2;
     uint64_t mix = 0;
 #pragma unroll
     for (int32_t k = 0; k < kHrMaxNgram; ++k)
-      if (k < n) mix ^= static_cast<uint64_t>(static_cast<int64_t>(cwin[j][k])) * mult[k];
-    const bool first = item == static_cast<int>(threadIdx.x);
-    const uint64_t prime = first ? prime_first : __ldg(h.primes + s);
-    const int64_t offset = first ? offset_first : __ldg(h.offsets + s);
+      if (k < n)
+        mix ^= static_cast<uint64_t>(static_cast<int64_t>(cwin[j][k])) *
+               (first ? mult[k] : __ldg(L.multipliers + k));
+    const uint64_t prime = first ? prime_first : __ldg(L.primes + s);
+    const int64_t offset = first ? offset_first : __ldg(L.offsets + s);
     const int32_t id = static_cast<int32_t>(static_cast<int64_t>(mix % prime) + offset);
     const int64_t i = bt * S + s;
-    if (h.hash_ids) h.hash_ids[i] = id;
-    uint4* dst = reinterpret_cast<uint4*>(a.rows + i * a.head_dim);
-    if (id < 0 || id >= a.num_rows) {
+    if (L.hash_ids) L.hash_ids[i] = id;
+    uint4* dst = reinterpret_cast<uint4*>(L.rows + i * a.head_dim);
+    if (id < 0 || id >= L.num_rows) {
       set_error(h.err, kErrIdRange);
       for (int32_t c = 0; c < 2 * chunks; ++c) dst[c] = make_uint4(0, 0, 0, 0);
       continue;
     }
     const uint4* src =
-        reinterpret_cast<const uint4*>(a.table + static_cast<int64_t>(id) * a.head_dim);
-    const uint8_t* sc = a.scales + static_cast<int64_t>(id) * (a.head_dim / 32);
+        reinterpret_cast<const uint4*>(L.table + static_cast<int64_t>(id) * a.head_dim);
+    const uint8_t* sc = L.scales + static_cast<int64_t>(id) * (a.head_dim / 32);
     if (chunks == 4) {   // head_dim 64: all four loads in flight at once
       uint4 code[4];
       uint32_t scl[2];
@@ -199,10 +216,25 @@ __global__ void __launch_bounds__(kHrThreads) hash_rows_kernel(HashRowsArgs a) {
   }
 }
 
+HashRowsArgs single_layer_hash_rows(const HashArgs& h, const uint8_t* table,
+                                    const uint8_t* scales, int64_t num_rows, int32_t head_dim,
+                                    uint16_t* rows) {
+  HashRowsArgs a{};
+  a.hash = h;
+  a.n_layers = 1;
+  a.head_dim = head_dim;
+  a.layer[0] = HashLayer{h.multipliers, h.primes, h.offsets, table, scales, num_rows, rows,
+                         h.hash_ids};
+  return a;
+}
+
 cudaError_t launch_hash_rows(const HashRowsArgs& a, cudaStream_t st, bool pdl) {
-  if (a.hash.max_ngram > kHrMaxNgram) return cudaErrorInvalidValue;
+  if (a.hash.max_ngram > kHrMaxNgram || a.n_layers < 1 || a.n_layers > kMaxHashLayers)
+    return cudaErrorInvalidValue;
+  const int32_t S = (a.hash.max_ngram - 1) * a.hash.n_heads;
   const int64_t M = static_cast<int64_t>(a.hash.B) * a.hash.T;
-  const int64_t blocks = (M + kHrPositions - 1) / kHrPositions;
+  const int32_t P = hash_rows_positions(a.n_layers * S);
+  const int64_t blocks = (M + P - 1) / P;
   return launch_ex(hash_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kHrThreads), 0, st,
                    pdl, a);
 }

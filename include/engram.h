@@ -111,6 +111,33 @@ typedef struct engram_weights {
   const uint16_t* k_weight;
 } engram_weights_t;
 
+/*
+ * One Engram layer's part in engram_hash_rows_layers. Each Engram layer takes its own entry of the
+ * hash layout (Engram listing, __init__: layer_hash_index = the layer's place in
+ * layout.layer_ids; its embedding has layout.num_embeddings[layer_hash_index] rows), so it has its
+ * own hash constants and table. All pointers are device pointers.
+ *   multipliers uint64 [max_ngram_size], primes uint64 [n_hash_cols], offsets int64 [n_hash_cols]:
+ *                  this layer's constants, with the meaning they have in engram_tables_t;
+ *   num_embeddings rows of this layer's table, in [1, 2^31);
+ *   table uint8 e4m3fn [num_embeddings, head_dim] (16-byte aligned), scales uint8 e8m0
+ *                  [num_embeddings, head_dim / 32]: this layer's embedding, as in engram_weights_t;
+ *   rows     out: bf16 [B * T, n_hash_cols * head_dim] (16-byte aligned), the layer's gathered and
+ *                  dequantised rows, i.e. the rows argument of engram_wkv_gate for this layer;
+ *   hash_ids out: int32 [B * T, n_hash_cols], or NULL.
+ */
+typedef struct engram_layer_hash {
+  const uint64_t* multipliers;
+  const uint64_t* primes;
+  const int64_t* offsets;
+  int64_t num_embeddings;
+  const uint8_t* table;
+  const uint8_t* scales;
+  uint16_t* rows;
+  int32_t* hash_ids;
+} engram_layer_hash_t;
+
+#define ENGRAM_MAX_HASH_LAYERS 16
+
 /* Message for the last non-OK status returned on this thread ("" if none). Never NULL. */
 ENGRAM_API const char* engram_last_error(void);
 
@@ -180,6 +207,32 @@ ENGRAM_API int engram_gate_and_add(const engram_desc_t* desc, const uint16_t* x,
                                    const uint16_t* kv, const uint16_t* q_weight,
                                    const uint16_t* k_weight, const uint8_t* token_mask,
                                    uint16_t* out, float* gate_out, int64_t M, void* stream);
+
+/*
+ * Stages 1 + 2 for several Engram layers in one launch (page "Module engram", stages 1 and 2;
+ * Engram listing, __init__: layer_hash_index; forward: self.embed(hash_ids)). A model's Engram
+ * layers all hash the same token stream: the window of compressed ids of each position (token
+ * map, look-back cache, pad) is resolved once and shared; each layer then forms its own slot ids
+ * with its own constants and gathers + dequantises its own rows, exactly as engram_hash followed
+ * by engram_embed_rows would for that layer. The cache is appended and cache_len advanced once
+ * (by T), as one engram_hash call would. Each layer's rows then feed engram_wkv_gate (or
+ * engram_wkv + engram_gate_and_add) with that layer's x.
+ *   desc: the geometry shared by the layers (n_heads, max_ngram_size, head_dim; num_embeddings
+ *         is not read, each layer gives its own);
+ *   tables: token_map, vocab and pad_id are used; multipliers, primes and offsets are not read
+ *           (they may be NULL);
+ *   layers: host array of n_layers (1 .. ENGRAM_MAX_HASH_LAYERS) layer records, read during the
+ *           call only; tokens, cache, cache_len, capacity as in engram_hash.
+ * Errors: as engram_hash and engram_embed_rows (an id outside a layer's [0, num_embeddings)
+ * writes a zero row and sets ENGRAM_DEVERR_ID_RANGE); n_layers out of range, a NULL or
+ * misaligned layer pointer, or outputs that overlap the cache return ENGRAM_EINVAL. B = 0 or
+ * T = 0 launches nothing.
+ */
+ENGRAM_API int engram_hash_rows_layers(const engram_desc_t* desc, const engram_tables_t* tables,
+                                       const engram_layer_hash_t* layers, int32_t n_layers,
+                                       const int32_t* tokens, int32_t B, int32_t T,
+                                       int32_t* cache, int32_t* cache_len, int32_t capacity,
+                                       void* stream);
 
 /*
  * Stages 3 + 4 in one tensor-core kernel (Engram listing, forward: self.wkv(...) followed by the

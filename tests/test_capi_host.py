@@ -114,3 +114,36 @@ def test_forward_workspace_and_validation(lib):
                             0x6000, 0x7000, 16, None, 0x900000, None, None, None, 0x1000000,
                             n16, None)
     assert rc == _lib.ENGRAM_EINVAL
+
+
+def test_hash_rows_layers_validation(lib):
+    d = desc()
+    t = _lib.EngramTables(0x1000, 1000, 0, None, None, None)   # per-layer constants not read
+
+    def layer(**kw):
+        f = dict(multipliers=0x2000, primes=0x3000, offsets=0x4000, num_embeddings=25874,
+                 table=0x10000, scales=0x20000, rows=0x40000, hash_ids=None)
+        f.update(kw)
+        return _lib.EngramLayerHash(**f)
+
+    def call(layers, n=None, B=2, T=3, cache=0x6000, cap=8):
+        arr = (_lib.EngramLayerHash * max(len(layers), 1))(*layers)
+        return lib.engram_hash_rows_layers(ctypes.byref(d), ctypes.byref(t), arr,
+                                           len(layers) if n is None else n, 0x5000, B, T, cache,
+                                           0x7000, cap, None)
+
+    ok = [layer(), layer(num_embeddings=30000, rows=0x80000)]
+    assert call(ok, B=0) == _lib.ENGRAM_OK                       # nothing to do
+    assert call(ok, n=0) == _lib.ENGRAM_EINVAL
+    assert call([layer()] * 17) == _lib.ENGRAM_EINVAL            # above ENGRAM_MAX_HASH_LAYERS
+    assert call([layer(), layer(table=None)]) == _lib.ENGRAM_EINVAL
+    assert b"layer 1" in lib.engram_last_error()
+    assert call([layer(rows=None)]) == _lib.ENGRAM_EINVAL
+    assert call([layer(rows=None)], B=0) == _lib.ENGRAM_OK       # no output when empty
+    assert call([layer(rows=0x40008)]) == _lib.ENGRAM_EINVAL     # rows not 16-byte aligned
+    assert call([layer(num_embeddings=1 << 31)]) == _lib.ENGRAM_EINVAL
+    assert call([layer(rows=0x6000)]) == _lib.ENGRAM_EINVAL      # rows overlap the cache
+    assert call([layer(hash_ids=0x6010)]) == _lib.ENGRAM_EINVAL  # ids overlap the cache
+    assert call(ok, B=-1) == _lib.ENGRAM_EINVAL
+    assert lib.engram_hash_rows_layers(ctypes.byref(d), ctypes.byref(t), None, 1, 0x5000, 2, 3,
+                                       0x6000, 0x7000, 8, None) == _lib.ENGRAM_EINVAL
