@@ -416,10 +416,99 @@ def run_configs(eg, desc, tables, weights, model, geom, flush, peaks):
         bound, frac = roofline_of(T, ms, peaks)
         sweep.append({"T": T, "value": round(T / (ms / 1e3), 1), "us_per_step": round(ms * 1e3, 2),
                       "bound": bound, "roofline_frac": round(frac, 4)})
+    res["layers"] = run_layers(eg, desc, tables, geom, flush, peaks)
+    res["layers"]["workload"] = ("stages 1+2 for 4 Engram layers (own constants and tables), one "
+                                 "launch vs one call per layer")
     res["sweep"] = {"workload": "prefill B1, T = 1 .. 65536", "unit": "tokens/s",
                     "points": sweep,
                     "crossover_tokens": round(WKV_BYTES / (FLOPS_PER_TOKEN / (peaks["bf16_tflops"]
                                               * 1e12) * peaks["hbm_gbs"] * 1e9 - BYTES_PER_TOKEN))}
+    return res
+
+
+def time_graph(fn, flush, steps, warmup):
+    """Mean ms of a captured CUDA graph of fn(), replayed per step with L2 flushed before each."""
+    import torch
+    graph = capture_graph(fn)
+    for _ in range(warmup):
+        flush.zero_()
+        graph.replay()
+    ev = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graph.replay()
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
+def run_layers(eg, desc, tables, geom, flush, peaks, n_layers=4, steps=20, warmup=3):
+    """Stages 1 + 2 for several Engram layers: n_layers layers (each with its own hash constants
+    and a 0.8-1.1 GB fp8 table) hashed and gathered by one engram_hash_rows_layers launch, against
+    one single-layer call per layer, each layer with its own copy of the look-back cache (what
+    separate per-layer hash states would do); at decode B64 (2048-token caches) and prefill B1
+    T4096. Algorithmic bytes per (token, layer): the 24 fp8 rows and their e8m0 scales read, the 24
+    bf16 rows written."""
+    import numpy as np
+    import torch
+    import synth
+
+    def dev(a):
+        a = np.ascontiguousarray(a)
+        return torch.from_numpy(a.view(np.int64) if a.dtype == np.uint64 else a).cuda()
+
+    S, hd = geom.n_hash_cols, geom.head_dim
+    layers = []
+    for i, lh in enumerate(synth.make_layer_hashes(geom, n_layers, synth.BASE_SEED + 800,
+                                                   with_tables=False)):
+        rows = lh.num_embeddings
+        layers.append(dict(
+            multipliers=dev(lh.multipliers), primes=dev(lh.primes), offsets=dev(lh.offsets),
+            table=synth.make_fp8_rows_device(rows, hd, synth.BASE_SEED + 810 + i),
+            scales=torch.full((rows, hd // 32), 127, dtype=torch.uint8, device="cuda")))
+    bytes_per = S * (hd + hd // 32 + 2 * hd)
+    res = {"n_layers": n_layers, "table_rows": [int(d["table"].shape[0]) for d in layers]}
+    rng = np.random.default_rng(synth.BASE_SEED + 820)
+    for name, B, T, prefill in (("decode_b64", 64, 1, 2048), ("prefill_b1_t4096", 1, 4096, 0)):
+        M = B * T
+        cap = prefill + T * (warmup + steps + 4)
+        tok = dev(synth.make_tokens(geom, B, T, rng))
+        caches = [(torch.zeros((B, cap), dtype=torch.int32, device="cuda"),
+                   torch.zeros(B, dtype=torch.int32, device="cuda")) for _ in range(n_layers + 1)]
+        recs = [eg.DeviceLayerHash(**d, rows=torch.empty((M, S * hd), dtype=torch.int16,
+                                                         device="cuda")) for d in layers]
+        if prefill:
+            pre = dev(synth.make_tokens(geom, B, prefill, rng))
+            pre_rows = torch.empty((B * prefill, S * hd), dtype=torch.int16, device="cuda")
+            for c, ln in caches:
+                eg.engram_hash_rows_layers(desc, tables, [eg.DeviceLayerHash(
+                    **layers[0], rows=pre_rows)], pre, c, ln)
+            del pre_rows
+
+        def shared():
+            eg.engram_hash_rows_layers(desc, tables, recs, tok, *caches[0])
+
+        def separate():
+            for i, r in enumerate(recs):
+                eg.engram_hash_rows_layers(desc, tables, [r], tok, *caches[i + 1])
+
+        ms_sh = time_graph(shared, flush, steps, warmup)
+        ms_sep = time_graph(separate, flush, steps, warmup)
+        if eg.engram_check_errors() != 0:
+            raise RuntimeError("device error word set during the layers workload")
+        nbytes = M * n_layers * bytes_per
+        gbs = nbytes / (ms_sh / 1e3) / 1e9
+        res[name] = {"tokens": M, "us_one_launch": round(ms_sh * 1e3, 2),
+                     "us_one_call_per_layer": round(ms_sep * 1e3, 2),
+                     "layer_tokens_per_s": round(M * n_layers / (ms_sh / 1e3), 1),
+                     "roofline": {"bound": "hbm", "achieved": round(gbs, 1),
+                                  "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                                  "frac": round(gbs / peaks["hbm_gbs"], 4),
+                                  "algorithmic_bytes": nbytes}}
+        del recs, caches
     return res
 
 
