@@ -149,8 +149,8 @@ constexpr size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 //  - kSmall:   M <= 256: weight-streaming projection over every SM (split-K partials in f32 when
 //              the workspace holds them, else bf16 kv), then the gate kernel;
 //  - kUnfused: the persistent projection GEMM into a bf16 kv, then the gate kernel; measured
-//              faster than the fused kernel below 1024 tokens (too few items to fill the GPU
-//              past the fused kernel's cold start);
+//              faster than the fused kernel below 640 tokens (too few items to fill the GPU
+//              past the fused kernel's cold start: 72 vs 74 us at 512, 86 vs 82 us at 640);
 //  - kFused:   projection + gate in one kernel; kv never touches HBM; least workspace.
 enum class Path { kDecode, kSmall, kUnfused, kFused };
 struct Plan {
@@ -158,7 +158,7 @@ struct Plan {
   int ksplit;
   size_t bytes;
 };
-constexpr int64_t kFusedMinTokens = 1024;
+constexpr int64_t kFusedMinTokens = 640;
 constexpr int kMaxPlans = 6;
 
 // Candidate plans in order of preference; returns how many were written.

@@ -279,8 +279,8 @@ ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64
  *   engram_forward_workspace_size for its size.
  * How stages 3 and 4 run depends on M and on the workspace given (the fastest path that fits):
  * up to 256 tokens, a weight-streaming projection over every SM (for up to 64 tokens, a fixed
- * share of the weight rows per SM) into a bf16 kv, then the gate kernel; below 1024 tokens, the
- * persistent projection GEMM into a bf16 kv then the gate kernel; from 1024 tokens, or when only
+ * share of the weight rows per SM) into a bf16 kv, then the gate kernel; below 640 tokens, the
+ * persistent projection GEMM into a bf16 kv then the gate kernel; from 640 tokens, or when only
  * the minimum workspace is given, the projection with the gate fused into its epilogue (as
  * engram_wkv_gate). Every path runs
  * on the GPU; results agree within the projection's f32-summation bound.

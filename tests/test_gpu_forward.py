@@ -134,7 +134,7 @@ def test_forward_unfused_geometry(odd, B, T):
 
 @pytest.mark.parametrize("ws_mode", ["fastest", "kv", "min"])
 @pytest.mark.parametrize("B,T,mask_frac", [(1, 1, 0.0), (2, 77, 0.0), (1, 300, 0.1),
-                                           (4, 160, 0.1), (64, 1, 0.0)])
+                                           (4, 160, 0.1), (64, 1, 0.0), (1, 700, 0.1)])
 def test_forward_full_width(wide, B, T, mask_frac, ws_mode):
     batch = synth.make_batch(wide.geom, B, T, synth.BASE_SEED + 200 + T, x_dist="student_t3",
                              mask_frac=mask_frac)

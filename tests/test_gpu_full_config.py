@@ -7,7 +7,7 @@ Full geometry (dim 5120, hc 4, 24 rows x head_dim 64) with the full ~805 MB fp8 
   * masked batched prefill B8 T8192 (pow2 scales, Student-t x, ~10% masked spans): a sample of
     tokens compared with the oracle, and every masked token checked bit for bit;
   * sweep end points T = 1 and T = 65536 (sampled).
-Runs of 1024 tokens and more take the fused kernel; their sampled tokens are re-run alone through
+Runs of 640 tokens and more take the fused kernel; their sampled tokens are re-run alone through
 engram_wkv_gate, which must reproduce them bit for bit and also returns the kv it used.
 """
 import numpy as np
