@@ -73,6 +73,8 @@ SIGNATURES = {
     "engram_forward_workspace_size": (_SZ, [_DESC, _I64]),
     "engram_forward": (ctypes.c_int, [_DESC, _TAB, _WTS, _P, _P, _I32, _I32, _P, _P, _I32, _P,
                                       _P, _P, _P, _P, _P, _SZ, _P]),
+    "engram_forward_ids": (ctypes.c_int, [_DESC, _WTS, _P, _P, _I64, _P, _P, _P, _P, _P, _SZ,
+                                          _P]),
     "engram_forward_noalloc": (ctypes.c_int, [_DESC, _TAB, _WTS, _P, _P, _I32, _I32, _P, _P,
                                               _I32, _P, _P, _P, _P, _P, _P]),
 }

@@ -206,6 +206,18 @@ def engram_forward(desc, tables: DeviceTables, weights: DeviceWeights, x, tokens
         _stream(stream)))
 
 
+def engram_forward_ids(desc, weights: DeviceWeights, x, hash_ids, token_mask, out, workspace,
+                       gate_out=None, kv_out=None, stream=None):
+    """Stages 2-4 from given hash ids [M, n_hash_cols] (the listing's forward(x, hash_ids, mask))."""
+    M = hash_ids.shape[0]
+    _check(lib().engram_forward_ids(
+        ctypes.byref(desc), ctypes.byref(weights.c), _ptr(x, "bf16", "x"),
+        _ptr(hash_ids, "i32", "hash_ids"), M, _ptr(token_mask, "u8", "token_mask"),
+        _ptr(out, "bf16", "out"), _ptr(gate_out, "f32", "gate_out"),
+        _ptr(kv_out, "bf16", "kv_out"), _ptr(workspace, "u8", "workspace"), workspace.numel(),
+        _stream(stream)))
+
+
 def engram_forward_noalloc(desc, tables: DeviceTables, weights: DeviceWeights, x, tokens, cache,
                            cache_len, token_mask, out, hash_ids_out=None, gate_out=None,
                            kv_out=None, stream=None):

@@ -32,6 +32,10 @@ int cuda_fail(cudaError_t e, const char* where) {
   return fail(ENGRAM_ECUDA, "%s: %s", where, cudaGetErrorString(e));
 }
 
+int cuda_fail(cudaError_t e, const char* who, const char* stage) {
+  return fail(ENGRAM_ECUDA, "%s: %s: %s", who, stage, cudaGetErrorString(e));
+}
+
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
 uint32_t* g_err_ptr[kMaxDevices] = {};
@@ -532,80 +536,65 @@ ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64
   return n > 0 ? plans[0].bytes : 0;
 }
 
-ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* tables,
-                              const engram_weights_t* wts, const uint16_t* x,
-                              const int32_t* tokens, int32_t B, int32_t T, int32_t* cache,
-                              int32_t* cache_len, int32_t capacity, const uint8_t* token_mask,
-                              uint16_t* out, int32_t* hash_ids_out, float* gate_out,
-                              uint16_t* kv_out, void* workspace, size_t workspace_bytes,
-                              void* stream) {
-  g_msg[0] = 0;
-  int rc = hash_checks(desc, tables, tokens, B, T, cache, cache_len, capacity, hash_ids_out,
-                       /*ids_optional=*/true);
-  if (rc) return rc;
-  const int64_t M = int64_t(B) * T;
+// Checks shared by the forward entry points (everything but the hash inputs); picks the fastest
+// plan whose scratch fits the workspace into *plan.
+static int forward_checks(const engram_desc_t* desc, const engram_weights_t* wts,
+                          const uint16_t* x, uint16_t* out, uint16_t* kv_out, int64_t M,
+                          void* workspace, size_t workspace_bytes, Plan* plan) {
   if (wts == nullptr) return fail(ENGRAM_EINVAL, "weights is NULL");
-  rc = gate_checks(desc, x, wts->wkv, wts->q_weight, wts->k_weight, out, M);
-  if (rc) return rc;
-  if (M == 0) return ENGRAM_OK;
+  int rc = gate_checks(desc, x, wts->wkv, wts->q_weight, wts->k_weight, out, M);
+  if (rc || M == 0) return rc;
   if (!wts->table || !wts->scales) return fail(ENGRAM_EINVAL, "NULL table");
   if (!aligned(wts->table, 16)) return fail(ENGRAM_EINVAL, "table must be 16-byte aligned");
   if (M >= (int64_t(1) << 31)) return fail(ENGRAM_EINVAL, "B * T too large");
-  const int S = n_hash_cols(desc);
-  const int32_t K = S * desc->head_dim;
+  const int32_t K = n_hash_cols(desc) * desc->head_dim;
   const int32_t N = desc->dim * (desc->hc_mult + 1);
   if (K % 64 != 0 || N % 32 != 0)
     return fail(ENGRAM_EUNSUPPORTED, "needs n_hash_cols * head_dim %% 64 == 0");
   if (kv_out && !aligned(kv_out, 16)) return fail(ENGRAM_EINVAL, "kv_out must be 16-byte aligned");
-  // the fastest plan whose scratch fits the workspace
   Plan plans[kMaxPlans];
   const int nplans = forward_plans(desc, M, plans);
-  const Plan* plan = nullptr;
+  const Plan* best = nullptr;
   size_t min_bytes = ~size_t(0);
   for (int i = 0; i < nplans; ++i) {
     if (plans[i].bytes < min_bytes) min_bytes = plans[i].bytes;
-    if (plan == nullptr && plans[i].bytes <= workspace_bytes) plan = &plans[i];
+    if (best == nullptr && plans[i].bytes <= workspace_bytes) best = &plans[i];
   }
-  if (workspace == nullptr || plan == nullptr || !aligned(workspace, 256))
+  if (workspace == nullptr || best == nullptr || !aligned(workspace, 256))
     return fail(ENGRAM_EINVAL,
                 "workspace must be 256-byte aligned and >= %zu bytes (%zu for the fastest path)",
                 min_bytes, nplans > 0 ? plans[0].bytes : size_t(0));
+  *plan = *best;
+  return ENGRAM_OK;
+}
 
+// Stages 3 + 4 of the forward by `plan`, on the gathered rows [M, K] at the start of the
+// workspace (its scratch follows them). The first kernel waits, through programmatic dependent
+// launch, for the kernel that wrote the rows; for the fused plan that kernel has also cleared
+// the fused kernel's counters.
+static int project_and_gate(const engram_desc_t* desc, const Plan& plan,
+                            const engram_weights_t* wts, const uint16_t* x,
+                            const uint8_t* token_mask, uint16_t* out, float* gate_out,
+                            uint16_t* kv_out, int64_t M, void* workspace, const LenAdvance& adv,
+                            uint32_t* err, cudaStream_t st, const char* who) {
+  const int32_t K = n_hash_cols(desc) * desc->head_dim;
+  const int32_t N = desc->dim * (desc->hc_mult + 1);
+  const uint16_t* rows = static_cast<const uint16_t*>(workspace);
+  uint8_t* ws = static_cast<uint8_t*>(workspace) + round256(size_t(M) * K * 2);
   cudaError_t e;
-  uint32_t* err = error_word(&e);
-  if (!err) return cuda_fail(e, "engram_forward");
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  uint16_t* rows = reinterpret_cast<uint16_t*>(ws);   // the projection's input [M, K]
-  HashArgs h = make_hash_args(desc, tables, tokens, B, T, cache, cache_len, capacity,
-                              hash_ids_out, err);
-  HashRowsArgs hr = single_layer_hash_rows(h, wts->table, wts->scales, desc->num_embeddings,
-                                           desc->head_dim, rows);
-  // the kernel that runs last advances the cache lengths (every reader of them is done)
-  const LenAdvance adv{cache_len, B, T, capacity};
-  const float inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));
-
-  // 1+2. hash every slot and gather its row into the projection's input, in one kernel. The
-  // kernels of the chain are launched with programmatic stream serialization: each overlaps its
-  // launch and prologue with the previous one and waits for it before touching its data.
-  ws += round256(size_t(M) * K * 2);
-  if (plan->path == Path::kFused)   // the fused kernel's counters, cleared by the hash kernel
-    fused_sync_region(ws, M, desc->hc_mult, desc->dim, &hr.zero, &hr.zero_n);
-  if ((e = launch_hash_rows(hr, st, true)) != cudaSuccess)
-    return cuda_fail(e, "engram_forward: hash + rows");
-  if (plan->path == Path::kFused) {
+  if (plan.path == Path::kFused) {
     // 3+4. projection with the gate fused into its epilogue
     FusedArgs f = make_fused_args(desc, rows, wts->wkv, x, wts->q_weight, wts->k_weight,
                                   token_mask, out, gate_out, kv_out, M, err);
     f.adv = adv;
     f.scratch = ws;
     f.sync_cleared = true;
-    if ((e = launch_fused(f, st, true)) != cudaSuccess) return cuda_fail(e, "engram_forward: fused");
+    if ((e = launch_fused(f, st, true)) != cudaSuccess) return cuda_fail(e, who, "fused");
     return ENGRAM_OK;
   }
   // 3. projection -> bf16 kv (or f32 split-K partials); 4. gate and add
   GateArgs ga{};
-  if (plan->path == Path::kDecode) {
+  if (plan.path == Path::kDecode) {
     WkvSmallArgs g{};
     g.a = rows;
     g.w = wts->wkv;
@@ -615,33 +604,31 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
     g.K = K;
     g.ksplit = 1;
     g.err = err;
-    if ((e = launch_wkv_decode(g, st, true)) != cudaSuccess)
-      return cuda_fail(e, "engram_forward: wkv");
+    if ((e = launch_wkv_decode(g, st, true)) != cudaSuccess) return cuda_fail(e, who, "wkv");
     ga.kv = g.kv;
-  } else if (plan->path == Path::kSmall) {
+  } else if (plan.path == Path::kSmall) {
     WkvSmallArgs g{};
     g.a = rows;
     g.w = wts->wkv;
     g.M = M;
     g.N = N;
     g.K = K;
-    g.ksplit = plan->ksplit;
+    g.ksplit = plan.ksplit;
     g.err = err;
-    if (plan->ksplit > 1) {
+    if (plan.ksplit > 1) {
       g.part = reinterpret_cast<float*>(ws);
       ga.part = g.part;
-      ga.ksplit = plan->ksplit;
+      ga.ksplit = plan.ksplit;
       ga.kv_out = kv_out;
     } else {
       g.kv = kv_out ? kv_out : reinterpret_cast<uint16_t*>(ws);
       ga.kv = g.kv;
     }
-    if ((e = launch_wkv_small(g, st, true)) != cudaSuccess)
-      return cuda_fail(e, "engram_forward: wkv");
+    if ((e = launch_wkv_small(g, st, true)) != cudaSuccess) return cuda_fail(e, who, "wkv");
   } else {
     uint16_t* kv = kv_out ? kv_out : reinterpret_cast<uint16_t*>(ws);
     WkvArgs g{rows, wts->wkv, kv, M, N, K, err};
-    if ((e = launch_wkv(g, st, true)) != cudaSuccess) return cuda_fail(e, "engram_forward: wkv");
+    if ((e = launch_wkv(g, st, true)) != cudaSuccess) return cuda_fail(e, who, "wkv");
     ga.kv = kv;
   }
   ga.x = x;
@@ -654,10 +641,91 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   ga.hc = desc->hc_mult;
   ga.dim = desc->dim;
   ga.eps = desc->norm_eps;
-  ga.inv_sqrt_dim = inv_sqrt_dim;
+  ga.inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));
   ga.adv = adv;
-  if ((e = launch_gate(ga, st, true)) != cudaSuccess) return cuda_fail(e, "engram_forward: gate");
+  if ((e = launch_gate(ga, st, true)) != cudaSuccess) return cuda_fail(e, who, "gate");
   return ENGRAM_OK;
+}
+
+ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* tables,
+                              const engram_weights_t* wts, const uint16_t* x,
+                              const int32_t* tokens, int32_t B, int32_t T, int32_t* cache,
+                              int32_t* cache_len, int32_t capacity, const uint8_t* token_mask,
+                              uint16_t* out, int32_t* hash_ids_out, float* gate_out,
+                              uint16_t* kv_out, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+  g_msg[0] = 0;
+  int rc = hash_checks(desc, tables, tokens, B, T, cache, cache_len, capacity, hash_ids_out,
+                       /*ids_optional=*/true);
+  if (rc) return rc;
+  const int64_t M = int64_t(B) * T;
+  Plan plan{};
+  rc = forward_checks(desc, wts, x, out, kv_out, M, workspace, workspace_bytes, &plan);
+  if (rc || M == 0) return rc;
+  cudaError_t e;
+  uint32_t* err = error_word(&e);
+  if (!err) return cuda_fail(e, "engram_forward");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint16_t* rows = static_cast<uint16_t*>(workspace);   // the projection's input [M, K]
+  HashArgs h = make_hash_args(desc, tables, tokens, B, T, cache, cache_len, capacity,
+                              hash_ids_out, err);
+  HashRowsArgs hr = single_layer_hash_rows(h, wts->table, wts->scales, desc->num_embeddings,
+                                           desc->head_dim, rows);
+  // 1+2. hash every slot and gather its row into the projection's input, in one kernel. The
+  // kernels of the chain are launched with programmatic stream serialization: each overlaps its
+  // launch and prologue with the previous one and waits for it before touching its data.
+  const int32_t K = n_hash_cols(desc) * desc->head_dim;
+  if (plan.path == Path::kFused)   // the fused kernel's counters, cleared by the hash kernel
+    fused_sync_region(static_cast<uint8_t*>(workspace) + round256(size_t(M) * K * 2), M,
+                      desc->hc_mult, desc->dim, &hr.zero, &hr.zero_n);
+  if ((e = launch_hash_rows(hr, st, true)) != cudaSuccess)
+    return cuda_fail(e, "engram_forward: hash + rows");
+  // 3+4; the kernel that runs last advances the cache lengths (every reader of them is done)
+  const LenAdvance adv{cache_len, B, T, capacity};
+  return project_and_gate(desc, plan, wts, x, token_mask, out, gate_out, kv_out, M, workspace,
+                          adv, err, st, "engram_forward");
+}
+
+ENGRAM_API int engram_forward_ids(const engram_desc_t* desc, const engram_weights_t* wts,
+                                  const uint16_t* x, const int32_t* hash_ids, int64_t M,
+                                  const uint8_t* token_mask, uint16_t* out, float* gate_out,
+                                  uint16_t* kv_out, void* workspace, size_t workspace_bytes,
+                                  void* stream) {
+  g_msg[0] = 0;
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (M < 0) return fail(ENGRAM_EINVAL, "M must be >= 0");
+  Plan plan{};
+  rc = forward_checks(desc, wts, x, out, kv_out, M, workspace, workspace_bytes, &plan);
+  if (rc || M == 0) return rc;
+  if (hash_ids == nullptr || !aligned(hash_ids, 4))
+    return fail(ENGRAM_EINVAL, "hash_ids must be a 4-byte aligned device array");
+  const int S = n_hash_cols(desc);
+  const int32_t K = S * desc->head_dim;
+  if (overlaps(hash_ids, size_t(M) * S * 4, workspace, round256(size_t(M) * K * 2)))
+    return fail(ENGRAM_EINVAL, "hash_ids overlaps the workspace");
+  cudaError_t e;
+  uint32_t* err = error_word(&e);
+  if (!err) return cuda_fail(e, "engram_forward_ids");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // 2. gather and dequantise the rows of every id into the projection's input
+  RowsArgs r{};
+  r.table = wts->table;
+  r.scales = wts->scales;
+  r.ids = hash_ids;
+  r.n_ids = M * S;
+  r.num_rows = desc->num_embeddings;
+  r.head_dim = desc->head_dim;
+  r.out = static_cast<uint16_t*>(workspace);
+  r.err = err;
+  if (plan.path == Path::kFused)   // the fused kernel's counters, cleared by the rows kernel
+    fused_sync_region(static_cast<uint8_t*>(workspace) + round256(size_t(M) * K * 2), M,
+                      desc->hc_mult, desc->dim, &r.zero, &r.zero_n);
+  if ((e = launch_rows(r, st, true)) != cudaSuccess)
+    return cuda_fail(e, "engram_forward_ids: rows");
+  const LenAdvance adv{nullptr, 0, 0, 0};
+  return project_and_gate(desc, plan, wts, x, token_mask, out, gate_out, kv_out, M, workspace,
+                          adv, err, st, "engram_forward_ids");
 }
 
 }  // extern "C"

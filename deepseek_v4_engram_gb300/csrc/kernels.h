@@ -80,6 +80,8 @@ struct RowsArgs {
   int32_t* adv_len;
   int32_t adv_B, adv_T, adv_cap;
   uint32_t* err;
+  int32_t* zero;          // optional: zero_n int32 set to 0 (the next kernel's counters)
+  int32_t zero_n;
 };
 
 struct GateArgs {
@@ -148,7 +150,7 @@ cudaError_t launch_hash_rows(const HashRowsArgs& a, cudaStream_t s, bool pdl);
 cudaError_t launch_hash(const HashArgs& a, cudaStream_t s);
 cudaError_t launch_advance_len(int32_t* cache_len, int32_t B, int32_t T, int32_t cap,
                                cudaStream_t s);
-cudaError_t launch_rows(const RowsArgs& a, cudaStream_t s);
+cudaError_t launch_rows(const RowsArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t s, bool pdl = false);
 bool small_supported(int64_t M, int32_t N, int32_t K);

@@ -72,6 +72,11 @@ cudaError_t launch_advance_len(int32_t* len, int32_t B, int32_t T, int32_t cap, 
 // Page "Module engram", stage 2 / embed_rows / regen_table: value * scale per 32-block, to bf16.
 
 __global__ void __launch_bounds__(256) rows_kernel(RowsArgs a) {
+  pdl_wait();   // the ids may come from the previous kernel of the stream
+  pdl_launch_dependents();
+  // the next kernel's counters (it reads them only after this grid has completed)
+  if (a.zero != nullptr && blockIdx.x == 0)
+    for (int32_t i = threadIdx.x; i < a.zero_n; i += blockDim.x) a.zero[i] = 0;
   if (a.adv_len != nullptr && blockIdx.x == 0) {
     for (int32_t b = threadIdx.x; b < a.adv_B; b += blockDim.x)
       a.adv_len[b] = min(a.adv_len[b] + a.adv_T, a.adv_cap);
@@ -239,13 +244,12 @@ cudaError_t launch_hash_rows(const HashRowsArgs& a, cudaStream_t st, bool pdl) {
                    pdl, a);
 }
 
-cudaError_t launch_rows(const RowsArgs& a, cudaStream_t st) {
+cudaError_t launch_rows(const RowsArgs& a, cudaStream_t st, bool pdl) {
   const int64_t total = a.n_ids * (a.head_dim / 16);
   int64_t blocks = (total + 255) / 256;
   if (blocks < 1) blocks = 1;
   if (blocks > (1 << 20)) blocks = 1 << 20;
-  rows_kernel<<<static_cast<unsigned>(blocks), 256, 0, st>>>(a);
-  return cudaGetLastError();
+  return launch_ex(rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(256), 0, st, pdl, a);
 }
 
 // -------------------------------------------------------------------- stage 4: gate and add

@@ -294,6 +294,25 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
                               void* stream);
 
 /*
+ * Stages 2-4 from hash ids computed elsewhere: the Engram listing's forward(x, hash_ids,
+ * token_mask) itself (Engram listing, forward; page "Module engram", stages 2-4). Gathers and
+ * dequantises the rows of hash_ids, projects, gates and adds, through the same token-count
+ * dependent paths as engram_forward (the ids may come from engram_hash, from
+ * engram_hash_rows_layers' hash_ids, or from the caller's own hash).
+ *   hash_ids int32 [M, n_hash_cols] (device, 4-byte aligned, not overlapping the workspace);
+ *   x bf16 [M, hc, dim]; token_mask uint8 [M] or NULL; out, gate_out, kv_out as in
+ *   engram_forward; workspace as in engram_forward (engram_forward_workspace_size(desc, M) bytes
+ *   for the fastest path, at least the same minimum).
+ * An id outside [0, num_embeddings) gathers a zero row and sets ENGRAM_DEVERR_ID_RANGE. M = 0
+ * launches nothing.
+ */
+ENGRAM_API int engram_forward_ids(const engram_desc_t* desc, const engram_weights_t* weights,
+                                  const uint16_t* x, const int32_t* hash_ids, int64_t M,
+                                  const uint8_t* token_mask, uint16_t* out, float* gate_out,
+                                  uint16_t* kv_out, void* workspace, size_t workspace_bytes,
+                                  void* stream);
+
+/*
  * engram_forward without a workspace argument, for callers that cannot allocate device memory
  * (a runtime that owns all device memory and passes a plugin only its inputs and outputs, or a
  * serving loop that must not call cudaMalloc, which can synchronise the device). The pages have

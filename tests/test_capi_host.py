@@ -147,3 +147,22 @@ def test_hash_rows_layers_validation(lib):
     assert call(ok, B=-1) == _lib.ENGRAM_EINVAL
     assert lib.engram_hash_rows_layers(ctypes.byref(d), ctypes.byref(t), None, 1, 0x5000, 2, 3,
                                        0x6000, 0x7000, 8, None) == _lib.ENGRAM_EINVAL
+
+
+def test_forward_ids_validation(lib):
+    d = desc()
+    w = _lib.EngramWeights(0x10000, 0x20000, 0x30000, 0x40000, 0x50000)
+    n16 = lib.engram_forward_workspace_size(ctypes.byref(d), 16)
+
+    def call(ids=0x8000, M=16, ws=0x1000000, nbytes=None, wts=w):
+        return lib.engram_forward_ids(ctypes.byref(d), None if wts is None else ctypes.byref(wts),
+                                      0x100000, ids, M, None, 0x900000, None, None, ws,
+                                      n16 if nbytes is None else nbytes, None)
+
+    assert call(M=-1) == _lib.ENGRAM_EINVAL
+    assert call(wts=None) == _lib.ENGRAM_EINVAL
+    assert call(nbytes=64) == _lib.ENGRAM_EINVAL and b"workspace" in lib.engram_last_error()
+    assert call(ids=None) == _lib.ENGRAM_EINVAL and b"hash_ids" in lib.engram_last_error()
+    assert call(ids=0x8002) == _lib.ENGRAM_EINVAL                       # misaligned ids
+    assert call(ids=0x1000000) == _lib.ENGRAM_EINVAL                    # ids inside the workspace
+    assert call(M=0, ids=None) == _lib.ENGRAM_OK                        # nothing to do

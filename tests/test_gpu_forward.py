@@ -159,3 +159,53 @@ def test_prefill_then_decode_equals_one_prefill(wide):
     np.testing.assert_array_equal(host(length), [T] * B)
     split = {k: np.concatenate([p[k] for p in parts], 1) for k in ("hash_ids", "out", "kv", "gate")}
     check_against_oracle(wide, batch, split)
+
+
+# ------------------------------------------------------------------ forward from given hash ids
+
+
+def run_forward_ids(dm, batch, ids, ws_mode):
+    B, T = batch.tokens.shape
+    g, M = dm.geom, batch.tokens.size
+    out = empty_bf16(M, g.hc_mult, g.dim)
+    gate = torch.full((M, g.hc_mult), float("nan"), device="cuda")
+    kv = empty_bf16(M, g.N)
+    mask = None if batch.mask is None else dev(batch.mask.reshape(M))
+    eg.engram_forward_ids(dm.desc, dm.weights, dev(batch.x.reshape(M, g.hc_mult, g.dim)),
+                          dev(np.ascontiguousarray(ids.reshape(M, -1), dtype=np.int32)), mask,
+                          out, ws_for(dm, M, ws_mode), gate_out=gate, kv_out=kv)
+    return host(out), host(gate), host(kv)
+
+
+@pytest.mark.parametrize("ws_mode", ["fastest", "min"])
+@pytest.mark.parametrize("B,T,mask_frac", [(1, 1, 0.0), (64, 1, 0.0), (2, 77, 0.1), (1, 300, 0.0),
+                                           (1, 700, 0.1)])
+def test_forward_ids_equals_forward(wide, B, T, mask_frac, ws_mode):
+    # the same ids through engram_forward_ids and engram_forward take the same kernels after the
+    # gather: bit-identical results; and both against the oracle
+    batch = synth.make_batch(wide.geom, B, T, synth.BASE_SEED + 900 + T, mask_frac=mask_frac)
+    r = run_forward(wide, batch, ws_mode=ws_mode)
+    out, gate, kv = run_forward_ids(wide, batch, r["hash_ids"], ws_mode)
+    assert eg.engram_check_errors() == 0
+    M = B * T
+    np.testing.assert_array_equal(out, r["out"].reshape(out.shape))
+    np.testing.assert_array_equal(gate, r["gate"].reshape(gate.shape))
+    np.testing.assert_array_equal(kv, r["kv"].reshape(kv.shape))
+    check_against_oracle(wide, batch, dict(out=out, gate=gate, kv=kv, hash_ids=r["hash_ids"]))
+
+
+@pytest.mark.parametrize("B,T", [(1, 5), (2, 150)])
+def test_forward_ids_unfused_geometry_and_bad_id(odd, B, T):
+    batch = synth.make_batch(odd.geom, B, T, synth.BASE_SEED + 950 + T, mask_frac=0.2)
+    st = E.NgramHashState(odd.model.tables.token_map, odd.model.tables.pad_id,
+                          odd.model.tables.multipliers, odd.model.tables.primes,
+                          odd.model.tables.offsets, odd.geom.n_heads, odd.geom.max_ngram_size, B)
+    ids = st.push(batch.tokens)
+    out, gate, kv = run_forward_ids(odd, batch, ids, "fastest")
+    assert eg.engram_check_errors() == 0
+    check_against_oracle(odd, batch, dict(out=out, gate=gate, kv=kv, hash_ids=ids))
+    # an id outside the table gathers a zero row and sets the error bit
+    bad = ids.copy()
+    bad[0, 0, 3] = odd.model.tables.num_embeddings
+    run_forward_ids(odd, batch, bad, "fastest")
+    assert eg.engram_check_errors() & 4
