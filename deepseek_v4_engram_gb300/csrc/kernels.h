@@ -53,6 +53,7 @@ struct HashRowsArgs {
   HashLayer layer[kMaxHashLayers];
   int32_t* zero;          // optional: zero_n int32 set to 0 (the next kernel's counters)
   int32_t zero_n;
+  int32_t positions;      // positions per block (set by launch_hash_rows)
 };
 
 // The single-layer form: layer 0 takes the constants and ids of `h` and the given table.

@@ -130,7 +130,7 @@ __global__ void __launch_bounds__(kHrThreads)
   const HashArgs& h = a.hash;
   const int32_t S = (h.max_ngram - 1) * h.n_heads;
   const int32_t LS = a.n_layers * S;   // items per position
-  const int32_t P = hash_rows_positions(LS);
+  const int32_t P = a.positions;
   const int64_t M = static_cast<int64_t>(h.B) * h.T;
   const int64_t pos0 = static_cast<int64_t>(blockIdx.x) * P;
   __shared__ int32_t cwin[kHrMaxPositions][kHrMaxNgram];
@@ -233,12 +233,27 @@ HashRowsArgs single_layer_hash_rows(const HashArgs& h, const uint8_t* table,
   return a;
 }
 
-cudaError_t launch_hash_rows(const HashRowsArgs& a, cudaStream_t st, bool pdl) {
-  if (a.hash.max_ngram > kHrMaxNgram || a.n_layers < 1 || a.n_layers > kMaxHashLayers)
+static int g_hr_sms = 0;
+
+cudaError_t launch_hash_rows(const HashRowsArgs& args, cudaStream_t st, bool pdl) {
+  if (args.hash.max_ngram > kHrMaxNgram || args.n_layers < 1 || args.n_layers > kMaxHashLayers)
     return cudaErrorInvalidValue;
+  if (g_hr_sms == 0) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&g_hr_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (g_hr_sms <= 0) g_hr_sms = 1;
+  }
+  HashRowsArgs a = args;
   const int32_t S = (a.hash.max_ngram - 1) * a.hash.n_heads;
   const int64_t M = static_cast<int64_t>(a.hash.B) * a.hash.T;
-  const int32_t P = hash_rows_positions(a.n_layers * S);
+  // As many positions per block as fit its threads, but no more than it takes to spread the
+  // positions over every SM: with few positions (decode) each SM then has few row loads in
+  // flight, which are latency-bound (a random 64-byte row of a large table each).
+  int64_t P = hash_rows_positions(a.n_layers * S);
+  const int64_t spread = (M + g_hr_sms - 1) / g_hr_sms;
+  if (spread < P) P = spread < 1 ? 1 : spread;
+  a.positions = static_cast<int32_t>(P);
   const int64_t blocks = (M + P - 1) / P;
   return launch_ex(hash_rows_kernel, dim3(static_cast<unsigned>(blocks)), dim3(kHrThreads), 0, st,
                    pdl, a);
