@@ -337,12 +337,15 @@ def capture_graph(fn):
     return graph
 
 
-def time_forward(eg, desc, tables, weights, x, tokens, mask, B, T, flush, steps, warmup):
+def time_forward(eg, desc, tables, weights, x, tokens, mask, B, T, flush, steps, warmup,
+                 in_graph=False):
     """Mean ms per step of engram_forward on B sequences of T new tokens: a captured graph
-    replayed per step, L2 flushed before each step (outside the events)."""
+    replayed per step, L2 flushed before each step (outside the events). With in_graph, also the
+    mean ms per step of 8 steps captured in one graph (time_steps_in_graph): (ms, ms or None)."""
     import torch
     M = B * T
-    cache = torch.zeros((B, T * (steps + warmup + 2)), dtype=torch.int32, device="cuda")
+    cache = torch.zeros((B, T * (steps + warmup + 2 + (40 if in_graph else 0))), dtype=torch.int32,
+                        device="cuda")
     cache_len = torch.zeros(B, dtype=torch.int32, device="cuda")
     out = torch.empty_like(x)
     ws = torch.empty(eg.engram_forward_workspace_size(desc, M), dtype=torch.uint8, device="cuda")
@@ -363,9 +366,11 @@ def time_forward(eg, desc, tables, weights, x, tokens, mask, B, T, flush, steps,
         b.record()
         ev.append((a, b))
     torch.cuda.synchronize()
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    ms_graph = time_steps_in_graph(step, flush, 8) if in_graph else None
     if eg.engram_check_errors() != 0:
         raise RuntimeError("device error word set")
-    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+    return (ms, ms_graph) if in_graph else ms
 
 
 def roofline_of(M, ms, peaks):
@@ -411,16 +416,25 @@ def run_configs(eg, desc, tables, weights, model, geom, flush, peaks):
     sweep = []
     for T in w["T_list"]:
         steps = 20 if T <= 4096 else 5
-        ms = time_forward(eg, desc, tables, weights, x_all[:, :T].contiguous(),
-                          tok_all[:, :T].contiguous(), None, 1, T, flush, steps=steps, warmup=3)
+        small = T <= 512   # where the graph launch per step is a visible share of the step
+        r = time_forward(eg, desc, tables, weights, x_all[:, :T].contiguous(),
+                         tok_all[:, :T].contiguous(), None, 1, T, flush, steps=steps, warmup=3,
+                         in_graph=small)
+        ms, ms_graph = r if small else (r, None)
         bound, frac = roofline_of(T, ms, peaks)
-        sweep.append({"T": T, "value": round(T / (ms / 1e3), 1), "us_per_step": round(ms * 1e3, 2),
-                      "bound": bound, "roofline_frac": round(frac, 4)})
+        point = {"T": T, "value": round(T / (ms / 1e3), 1), "us_per_step": round(ms * 1e3, 2),
+                 "bound": bound, "roofline_frac": round(frac, 4)}
+        if ms_graph is not None:
+            point["in_graph"] = {"us_per_step": round(ms_graph * 1e3, 2),
+                                 "roofline_frac": round(roofline_of(T, ms_graph, peaks)[1], 4)}
+        sweep.append(point)
     res["layers"] = run_layers(eg, desc, tables, geom, flush, peaks)
     res["layers"]["workload"] = ("stages 1+2 for 4 Engram layers (own constants and tables), one "
                                  "launch vs one call per layer")
     res["sweep"] = {"workload": "prefill B1, T = 1 .. 65536", "unit": "tokens/s",
                     "points": sweep,
+                    "in_graph_timing": "T <= 512: also 8 steps in one CUDA graph, L2 flushed "
+                                       "before each, event record nodes around each step",
                     "crossover_tokens": round(WKV_BYTES / (FLOPS_PER_TOKEN / (peaks["bf16_tflops"]
                                               * 1e12) * peaks["hbm_gbs"] * 1e9 - BYTES_PER_TOKEN))}
     return res
@@ -522,7 +536,7 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
     rng = np.random.default_rng(synth.BASE_SEED + 102)
     n = args.warmup + args.steps + 4
     pre = torch.from_numpy(rng.integers(0, geom.vocab, (B, prefill), dtype=np.int32)).cuda()
-    cache = torch.zeros((B, prefill + n), dtype=torch.int32, device="cuda")
+    cache = torch.zeros((B, prefill + n + 64), dtype=torch.int32, device="cuda")
     cache_len = torch.zeros(B, dtype=torch.int32, device="cuda")
     ids = torch.empty((B, prefill, geom.n_hash_cols), dtype=torch.int32, device="cuda")
     eg.engram_hash(desc, tables, pre, cache, cache_len, ids)
@@ -550,16 +564,53 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
         times.append((a, b))
     torch.cuda.synchronize()
     ms = statistics.mean(a.elapsed_time(b) for a, b in times)
+    in_graph_ms = time_steps_in_graph(step, flush, 8)
     if eg.engram_check_errors() != 0:
         raise RuntimeError("device error word set during decode")
     bytes_step = WKV_BYTES + B * BYTES_PER_TOKEN
     gbs = bytes_step / (ms / 1e3) / 1e9
-    return {"workload": f"decode B{B} x 1 token, {prefill}-token cache per sequence",
-            "value": round(B / (ms / 1e3), 1), "unit": "tokens/s", "us_per_step": round(ms * 1e3, 2),
-            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
-                         "algorithmic_bytes": bytes_step},
-            "gpu_launches_per_step": 3, "timing": "CUDA graph replay per step, L2 flushed"}
+    res = {"workload": f"decode B{B} x 1 token, {prefill}-token cache per sequence",
+           "value": round(B / (ms / 1e3), 1), "unit": "tokens/s", "us_per_step": round(ms * 1e3, 2),
+           "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                        "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
+                        "algorithmic_bytes": bytes_step},
+           "gpu_launches_per_step": 3, "timing": "CUDA graph replay per step, L2 flushed"}
+    if in_graph_ms is not None:
+        # the same steps without a graph launch per step: what a serving loop that captures many
+        # layers or steps in one graph sees
+        res["in_graph"] = {
+            "us_per_step": round(in_graph_ms * 1e3, 2),
+            "frac": round(bytes_step / (in_graph_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+            "timing": "8 steps in one CUDA graph, L2 flushed (256 MB write) before each, event "
+                      "record nodes around each step"}
+    return res
+
+
+def time_steps_in_graph(step, flush, k, replays=3):
+    """Mean ms per step of `step` captured k times in one CUDA graph, each preceded by an L2
+    flush and bracketed by event record nodes (events recorded inside the graph), so that the
+    per-step time excludes the graph launch. None where torch cannot record events in a graph."""
+    import torch
+    try:
+        evs = [(torch.cuda.Event(enable_timing=True, external=True),
+                torch.cuda.Event(enable_timing=True, external=True)) for _ in range(k)]
+    except TypeError:
+        return None
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for a, b in evs:
+            flush.zero_()
+            a.record()
+            step()
+            b.record()
+    graph.replay()   # warm-up
+    torch.cuda.synchronize()
+    samples = []
+    for _ in range(replays):
+        graph.replay()
+        torch.cuda.synchronize()
+        samples += [a.elapsed_time(b) for a, b in evs]
+    return statistics.mean(samples)
 
 
 def run_e2e(eg, desc, tables, weights, batch, geom, args, world):
