@@ -209,3 +209,19 @@ def test_forward_ids_unfused_geometry_and_bad_id(odd, B, T):
     bad[0, 0, 3] = odd.model.tables.num_embeddings
     run_forward_ids(odd, batch, bad, "fastest")
     assert eg.engram_check_errors() & 4
+
+
+@pytest.mark.parametrize("B,T", [(64, 1), (1, 300), (1, 700)])
+def test_forward_degenerate_masks(wide, B, T):
+    # every token masked (an all-image batch): out is x bit for bit and every gate is 0; an
+    # explicit all-True mask gives bit for bit what no mask gives. Decode, unfused and fused paths.
+    import dataclasses
+    batch = synth.make_batch(wide.geom, B, T, synth.BASE_SEED + 970 + T)
+    none = run_forward(wide, batch)
+    all_true = run_forward(wide, dataclasses.replace(batch, mask=np.ones((B, T), dtype=bool)))
+    for key in ("out", "gate", "kv", "hash_ids"):
+        np.testing.assert_array_equal(all_true[key], none[key])
+    masked = run_forward(wide, dataclasses.replace(batch, mask=np.zeros((B, T), dtype=bool)))
+    np.testing.assert_array_equal(masked["out"].reshape(batch.x.shape), batch.x)
+    assert (masked["gate"] == 0).all()
+    np.testing.assert_array_equal(masked["kv"], none["kv"])   # the projection ignores the mask
