@@ -38,6 +38,19 @@ int cuda_fail(cudaError_t e, const char* who, const char* stage) {
 
 constexpr int kMaxDevices = 64;
 std::mutex g_mu;
+
+// Per-device host state (device_sm_count, ensure_dynamic_smem, fused_resident_pairs_cached).
+std::mutex g_dev_mu;
+int g_sm_count[kMaxDevices] = {};
+int g_fused_pairs[kMaxDevices] = {};
+constexpr int kMaxSmemKernels = 16;
+const void* g_smem_kernel[kMaxDevices][kMaxSmemKernels] = {};
+
+int current_device() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) dev = 0;
+  return dev;
+}
 uint32_t* g_err_ptr[kMaxDevices] = {};
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 
@@ -204,6 +217,44 @@ bool have_encoder() {
   return true;
 }
 }  // namespace
+
+int device_sm_count() {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  if (g_sm_count[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 1;
+    g_sm_count[dev] = n;
+  }
+  return g_sm_count[dev];
+}
+
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes) {
+  const int dev = current_device();
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  int free_slot = -1;
+  for (int i = 0; i < kMaxSmemKernels; ++i) {
+    if (g_smem_kernel[dev][i] == kernel) return cudaSuccess;
+    if (g_smem_kernel[dev][i] == nullptr && free_slot < 0) free_slot = i;
+  }
+  const cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(bytes));
+  if (e == cudaSuccess && free_slot >= 0) g_smem_kernel[dev][free_slot] = kernel;
+  return e;
+}
+
+int fused_resident_pairs_cached(int (*query)()) {
+  const int dev = current_device();
+  {
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    if (g_fused_pairs[dev] > 0) return g_fused_pairs[dev];
+  }
+  const int n = query();   // needs the kernel's shared-memory limit raised (its own lock)
+  std::lock_guard<std::mutex> lock(g_dev_mu);
+  g_fused_pairs[dev] = n;
+  return n;
+}
 
 bool tensor_map_3d_bf16(void* map_out, const void* base, uint64_t d0, uint64_t d1, uint64_t d2,
                         uint32_t box0, uint32_t box1, uint32_t box2) {

@@ -192,17 +192,7 @@ __global__ void __launch_bounds__(kDecThreads, 1)
   }
 }
 
-int g_dec_sms = 0;
-
-int dec_sm_count() {
-  if (g_dec_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_dec_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_dec_sms <= 0) g_dec_sms = 1;
-  }
-  return g_dec_sms;
-}
+int dec_sm_count() { return device_sm_count(); }
 
 }  // namespace
 
@@ -220,14 +210,9 @@ cudaError_t launch_wkv_decode(const WkvSmallArgs& a, cudaStream_t st, bool pdl) 
   if (!tensor_map_2d_bf16(&tmW, a.w, a.K, a.N, kBK, kDecRows) ||
       !tensor_map_2d_bf16(&tmA, a.a, a.K, M, kBK, nt))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(wkv_decode_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(decode_smem_bytes()));
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(wkv_decode_kernel),
+                                            decode_smem_bytes());
+  if (e != cudaSuccess) return e;
   DecParams p{};
   p.kv = a.kv;
   p.M = M;

@@ -686,29 +686,27 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   }
 }
 
-int g_max_pairs = 0;
-
-// Largest number of CTA pairs of this kernel that can be resident at once.
-int max_resident_pairs() {
-  if (g_max_pairs == 0) {
-    cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(2, 1, 1);
-    cfg.blockDim = dim3(kFusedThreads, 1, 1);
-    cfg.dynamicSmemBytes = fused_smem_bytes();
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    if (cudaOccupancyMaxActiveClusters(&n, engram_fused_kernel, &cfg) != cudaSuccess || n <= 0)
-      n = 1;
-    g_max_pairs = n;
-  }
-  return g_max_pairs;
+// Largest number of CTA pairs of this kernel that can be resident at once on the current device
+// (the kernel's shared-memory limit must have been raised first).
+int query_resident_pairs() {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2, 1, 1);
+  cfg.blockDim = dim3(kFusedThreads, 1, 1);
+  cfg.dynamicSmemBytes = fused_smem_bytes();
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, engram_fused_kernel, &cfg) != cudaSuccess || n <= 0)
+    n = 1;
+  return n;
 }
+
+int max_resident_pairs() { return fused_resident_pairs_cached(query_resident_pairs); }
 
 size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
@@ -756,13 +754,10 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl) {
       !tensor_map_3d_bf16(&tmX, a.x, a.dim, a.hc, a.M, kXCols, 1, kBM) ||
       !tensor_map_3d_bf16(&tmOut, a.out, a.dim, a.hc, a.M, kXCols, 1, kBM))
     return cudaErrorInvalidValue;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(engram_fused_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(fused_smem_bytes()));
+  {
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(engram_fused_kernel),
+                                              fused_smem_bytes());
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const ScratchLayout l = scratch_layout(a.M, a.hc, a.dim);
   uint8_t* base = static_cast<uint8_t*>(a.scratch);

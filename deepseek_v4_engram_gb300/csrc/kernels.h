@@ -181,6 +181,16 @@ cudaError_t launch_ex(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sm
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
+// Host-side state per device (capi.cu), thread-safe: the current device's SM count, and raising
+// a kernel's dynamic shared-memory limit once per (device, kernel) (the limit is a property of
+// the function on each device, so a process that drives several GPUs needs it on every one).
+int device_sm_count();
+cudaError_t ensure_dynamic_smem(const void* kernel, size_t bytes);
+
+// The fused kernel's resident CTA pairs on the current device (forward_sm103.cu), cached per
+// device.
+int fused_resident_pairs_cached(int (*query)());
+
 // Smallest workspace engram_forward accepts for M tokens (the fused path's, where it applies).
 size_t forward_min_workspace_bytes(const engram_desc_t* desc, int64_t M);
 

@@ -193,16 +193,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
   }
 }
 
-int g_sms = 0;
-int sm_count() {
-  if (g_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_sms <= 0) g_sms = 1;
-  }
-  return g_sms;
-}
+int sm_count() { return device_sm_count(); }
 
 }  // namespace
 
@@ -239,13 +230,10 @@ cudaError_t launch_wkv_small(const WkvSmallArgs& a, cudaStream_t st, bool pdl) {
   int stages = kSmallSmemBudget / stage_bytes;
   if (stages > kSmallMaxStages) stages = kSmallMaxStages;
   const size_t smem = size_t(stages) * stage_bytes + sizeof(SmallShared) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(wkv_small_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kSmallSmemBudget + int(sizeof(SmallShared)) + 2048);
+  {
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(wkv_small_kernel),
+                                              kSmallSmemBudget + sizeof(SmallShared) + 2048);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   SmallParams p{};
   p.kv = a.kv;

@@ -233,17 +233,9 @@ HashRowsArgs single_layer_hash_rows(const HashArgs& h, const uint8_t* table,
   return a;
 }
 
-static int g_hr_sms = 0;
-
 cudaError_t launch_hash_rows(const HashRowsArgs& args, cudaStream_t st, bool pdl) {
   if (args.hash.max_ngram > kHrMaxNgram || args.n_layers < 1 || args.n_layers > kMaxHashLayers)
     return cudaErrorInvalidValue;
-  if (g_hr_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_hr_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_hr_sms <= 0) g_hr_sms = 1;
-  }
   HashRowsArgs a = args;
   const int32_t S = (a.hash.max_ngram - 1) * a.hash.n_heads;
   const int64_t M = static_cast<int64_t>(a.hash.B) * a.hash.T;
@@ -251,7 +243,8 @@ cudaError_t launch_hash_rows(const HashRowsArgs& args, cudaStream_t st, bool pdl
   // positions over every SM: with few positions (decode) each SM then has few row loads in
   // flight, which are latency-bound (a random 64-byte row of a large table each).
   int64_t P = hash_rows_positions(a.n_layers * S);
-  const int64_t spread = (M + g_hr_sms - 1) / g_hr_sms;
+  const int64_t sms = device_sm_count();
+  const int64_t spread = (M + sms - 1) / sms;
   if (spread < P) P = spread < 1 ? 1 : spread;
   a.positions = static_cast<int32_t>(P);
   const int64_t blocks = (M + P - 1) / P;

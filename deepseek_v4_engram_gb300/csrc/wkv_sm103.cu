@@ -161,17 +161,7 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
   }
 }
 
-int g_num_sms = 0;
-
-int num_sms() {
-  if (g_num_sms == 0) {
-    int dev = 0;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&g_num_sms, cudaDevAttrMultiProcessorCount, dev);
-    if (g_num_sms <= 0) g_num_sms = 1;
-  }
-  return g_num_sms;
-}
+int num_sms() { return device_sm_count(); }
 
 }  // namespace
 
@@ -180,12 +170,9 @@ cudaError_t launch_wkv(const WkvArgs& a, cudaStream_t st, bool pdl) {
   if (!tensor_map_2d_bf16(&tmA, a.a, a.K, a.M, kBK, kBM)) return cudaErrorInvalidValue;
   if (!tensor_map_2d_bf16(&tmB, a.w, a.K, a.N, kBK, kBN)) return cudaErrorInvalidValue;
   const size_t smem = kStages * (kTileABytes + kTileBBytes) + sizeof(GemmShared) + 1024;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(wkv_gemm_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+  {
+    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(wkv_gemm_kernel), smem);
     if (e != cudaSuccess) return e;
-    attr_set = true;
   }
   const int64_t tiles = ((a.M + kBM - 1) / kBM) * ((a.N + kBN - 1) / kBN);
   const int grid = static_cast<int>(tiles < num_sms() ? tiles : num_sms());
