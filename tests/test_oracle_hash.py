@@ -145,3 +145,34 @@ def test_slot_dependence_on_lookbacks():
     np.testing.assert_array_equal(r_p2[:8], r0[:8])
     assert (r_p2[8:] != r0[8:]).sum() >= 12
     assert (r_p1 != r0).sum() >= 18
+
+
+def test_brute_force_every_window_of_a_tiny_vocabulary():
+    # Every window over 5 compressed ids, at every distance from the sequence start (so with 0
+    # to 3 pad look-backs), against the formula evaluated in Python integers: for n = 2..4,
+    # mix_n = XOR over k < n of (c_{p-k} * m_k mod 2^64), id = mix_n mod P_s + O_s. Generic odd
+    # 64-bit multipliers exercise the wrap and the unsigned modulo on every slot.
+    import itertools
+    rng = np.random.default_rng(6)
+    V, pad = 5, 3
+    token_map = np.array([4, 0, 2, 1, 3], dtype=np.int64)   # a permutation: tokens != ids
+    mults = [int(v) * 2 + 1 for v in rng.integers(0, 2 ** 63, size=NMAX, dtype=np.int64)]
+    primes = synth.consecutive_primes(1009, S)
+    offsets = [0] + list(np.cumsum([int(p) for p in primes[:-1]]))
+    checked = 0
+    for length in range(1, NMAX + 1):          # the last position p = length - 1
+        for toks in itertools.product(range(V), repeat=length):
+            st, _ = state(token_map, np.array(mults, dtype=np.uint64), primes, pad=pad)
+            got = st.push(np.array([toks], dtype=np.int64))[0, -1]
+            c = [int(token_map[t]) for t in toks]
+            p = length - 1
+            for n in range(2, NMAX + 1):
+                mix = 0
+                for k in range(n):
+                    ck = c[p - k] if p - k >= 0 else pad
+                    mix ^= (ck * mults[k]) % (1 << 64)
+                for head in range(H):
+                    s = (n - 2) * H + head
+                    assert int(got[s]) == mix % int(primes[s]) + int(offsets[s]), (toks, s)
+            checked += 1
+    assert checked == sum(V ** L for L in range(1, NMAX + 1))
