@@ -29,6 +29,10 @@
  *  - engram_last_error() gives a message for the last non-OK return on the calling thread.
  *  - Calls that are in flight at the same time on different streams must not share output or
  *    cache buffers.
+ *  - Calls may come from several host threads and for several devices (each call runs on the
+ *    device current on its thread). The library's host-side state (the device error word, SM
+ *    counts, kernel attributes) is kept per device and guarded; the error word is shared by all
+ *    calls on one device.
  */
 #ifndef ENGRAM_H_
 #define ENGRAM_H_
