@@ -53,11 +53,13 @@ def run(dm, batch, noalloc: bool):
 
 def test_noalloc_matches_workspace_forward_on_consecutive_calls(wide):
     g = wide.geom
-    # two calls in a row with different inputs and sizes: the second overwrites the first's
-    # scratch; both must match engram_forward with a caller-provided workspace
+    # calls in a row with different inputs and sizes (the unfused projection at 600 tokens, the
+    # small-batch one at 231, the fused kernel at 1024): each overwrites the previous one's
+    # scratch; all must match engram_forward with a caller-provided workspace
     batches = [synth.make_batch(g, 2, 300, synth.BASE_SEED + 500, x_dist="student_t3",
                                 mask_frac=0.1),
-               synth.make_batch(g, 3, 77, synth.BASE_SEED + 501)]
+               synth.make_batch(g, 3, 77, synth.BASE_SEED + 501),
+               synth.make_batch(g, 1, 1024, synth.BASE_SEED + 502, mask_frac=0.1)]
     got = [run(wide, b, noalloc=True) for b in batches]
     for b, (out, ids, gate, length, _) in zip(batches, got):
         ref_out, ref_ids, ref_gate, ref_len, ref_kv = run(wide, b, noalloc=False)
