@@ -574,7 +574,10 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                         "algorithmic_bytes": bytes_step},
-           "gpu_launches_per_step": 3, "timing": "CUDA graph replay per step, L2 flushed"}
+           "gpu_launches_per_step": 2,
+           "kernels": "engram_decode_kernel (hash + gather + projection in every CTA), "
+                      "gate_part_kernel",
+           "timing": "CUDA graph replay per step, L2 flushed"}
     if in_graph_ms is not None:
         # the same steps without a graph launch per step: what a serving loop that captures many
         # layers or steps in one graph sees
