@@ -549,21 +549,7 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
     def step():
         eg.engram_forward(desc, tables, weights, x, tok, cache, cache_len, None, out, ws)
 
-    graph = capture_graph(step)
-    for _ in range(args.warmup):
-        flush.zero_()
-        graph.replay()
-    torch.cuda.synchronize()
-    times = []
-    for _ in range(args.steps):
-        flush.zero_()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        graph.replay()
-        b.record()
-        times.append((a, b))
-    torch.cuda.synchronize()
-    ms = statistics.mean(a.elapsed_time(b) for a, b in times)
+    ms = time_graph(step, flush, args.steps, args.warmup)
     in_graph_ms = time_steps_in_graph(step, flush, 8)
     if eg.engram_check_errors() != 0:
         raise RuntimeError("device error word set during decode")
@@ -574,10 +560,21 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                         "algorithmic_bytes": bytes_step},
-           "gpu_launches_per_step": 2,
-           "kernels": "engram_decode_kernel (hash + gather + projection in every CTA), "
-                      "gate_part_kernel",
-           "timing": "CUDA graph replay per step, L2 flushed"}
+           "gpu_launches_per_step": 3, "timing": "CUDA graph replay per step, L2 flushed "
+                                                 "(256 MB write) before each"}
+    # The floor a step meets in this setting: one cold read of the 78.6 MB weight by a plain
+    # torch reduction after the same flush. The flush leaves L2 full of dirty lines, so every
+    # line the read brings in also writes one back: the read moves about twice its bytes.
+    wv = weights.wkv.view(torch.float32).view(-1)
+    red = torch.empty((), dtype=torch.float32, device="cuda")
+    floor_ms = time_graph(lambda: torch.sum(wv, dim=0, out=red), flush, args.steps, args.warmup)
+    res["weight_read_floor"] = {
+        "us": round(floor_ms * 1e3, 2),
+        "frac_of_hbm_peak": round(WKV_BYTES / (floor_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+        "timing": "torch.sum over the wkv weight (78.6 MB, its f32 view flattened), CUDA "
+                  "graph replay, L2 flushed before each as for the steps"}
+    res["inputs_larger_than_l2"] = decode_rotating(eg, desc, tables, weights, geom, cache,
+                                                   cache_len, B, args, peaks, bytes_step)
     if in_graph_ms is not None:
         # the same steps without a graph launch per step: what a serving loop that captures many
         # layers or steps in one graph sees
@@ -587,6 +584,57 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
             "timing": "8 steps in one CUDA graph, L2 flushed (256 MB write) before each, event "
                       "record nodes around each step"}
     return res
+
+
+def decode_rotating(eg, desc, tables, weights, geom, cache, cache_len, B, args, peaks,
+                    bytes_step, copies=3):
+    """The decode step with no flush between steps: each step reads its own copy of the wkv
+    weight, x and tokens, and the copies rotate, so the inputs of the steps add up to more than
+    L2 (3 x 78.6 MB of weight): every step reads its weight from HBM, and L2 holds no dirty lines
+    from a flush (as in a model, where a decode step streams other layers' weights in between)."""
+    import numpy as np
+    import torch
+    import synth
+    graphs = []
+    keep = []
+    for c in range(copies):
+        w = weights.wkv.clone()
+        wts = eg.DeviceWeights(weights.table, weights.scales, w, weights.q_weight,
+                               weights.k_weight)
+        batch = synth.make_batch(geom, B, 1, synth.BASE_SEED + 710 + c)
+        x = torch.from_numpy(batch.x.view(np.int16)).cuda()
+        tok = torch.from_numpy(batch.tokens).cuda()
+        out = torch.empty_like(x)
+        ws = torch.empty(eg.engram_forward_workspace_size(desc, B), dtype=torch.uint8,
+                         device="cuda")
+        keep.append((w, wts, x, tok, out, ws))
+
+        def step(wts=wts, x=x, tok=tok, out=out, ws=ws):
+            eg.engram_forward(desc, tables, wts, x, tok, cache, cache_len, None, out, ws)
+        graphs.append(capture_graph(step))
+    for i in range(args.warmup * copies):
+        graphs[i % copies].replay()
+    torch.cuda.synchronize()
+    ev = []
+    n = args.steps - args.steps % copies or copies
+    for i in range(n):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        graphs[i % copies].replay()
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    if eg.engram_check_errors() != 0:
+        raise RuntimeError("device error word set during decode")
+    ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
+    gbs = bytes_step / (ms / 1e3) / 1e9
+    del keep
+    return {"value": round(B / (ms / 1e3), 1), "unit": "tokens/s",
+            "us_per_step": round(ms * 1e3, 2),
+            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4)},
+            "timing": f"CUDA graph replay per step, no flush: {copies} copies of the weight, x "
+                      "and tokens rotated (inputs larger than L2)"}
 
 
 def time_steps_in_graph(step, flush, k, replays=3):

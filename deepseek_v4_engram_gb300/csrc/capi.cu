@@ -9,7 +9,6 @@
 #include <cudaTypedefs.h>
 
 #include "engram.h"
-#include "decode_step.h"
 #include "kernels.h"
 
 namespace engram {
@@ -162,9 +161,6 @@ HashArgs make_hash_args(const engram_desc_t* d, const engram_tables_t* t, const 
 constexpr size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 
 // How engram_forward runs stages 3 and 4 for a given token count, fastest first:
-//  - kDecodeStep: M <= 64 at head_dim 64: one kernel hashes and gathers inside every CTA while
-//              the weight streams in (64-row units, a fixed share per SM), and leaves key partial
-//              sums and value rows for the gate kernel; stages 1 and 2 are part of it;
 //  - kDecode:  M <= 64: weight-streaming projection in 64-row units, a fixed share per SM, into
 //              a bf16 kv (no partial sums), then the gate kernel;
 //  - kSmall:   M <= 256: weight-streaming projection over every SM (split-K partials in f32 when
@@ -173,14 +169,14 @@ constexpr size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 //              faster than the fused kernel below 640 tokens (too few items to fill the GPU
 //              past the fused kernel's cold start: 72 vs 74 us at 512, 86 vs 82 us at 640);
 //  - kFused:   projection + gate in one kernel; kv never touches HBM; least workspace.
-enum class Path { kDecodeStep, kDecode, kSmall, kUnfused, kFused };
+enum class Path { kDecode, kSmall, kUnfused, kFused };
 struct Plan {
   Path path;
   int ksplit;
   size_t bytes;
 };
 constexpr int64_t kFusedMinTokens = 640;
-constexpr int kMaxPlans = 8;
+constexpr int kMaxPlans = 6;
 
 // Candidate plans in order of preference; returns how many were written.
 int forward_plans(const engram_desc_t* d, int64_t M, Plan* out) {
@@ -191,11 +187,6 @@ int forward_plans(const engram_desc_t* d, int64_t M, Plan* out) {
   const size_t kv_bytes = round256(size_t(M) * N * 2);
   const bool fused = fused_supported(K, d->hc_mult, d->dim);
   int n = 0;
-  const DecodeGeometry dg{d->dim, d->hc_mult, d->n_heads, d->max_ngram_size, d->head_dim};
-  if (decode_step_supported(M, dg))   // no gathered rows: partial sums and value rows only
-    out[n++] = {Path::kDecodeStep, 1,
-                round256(decode_step_part_bytes(d->hc_mult, d->dim)) +
-                    round256(size_t(M) * d->dim * 2)};
   if (decode_supported(M, N, K)) out[n++] = {Path::kDecode, 1, base + kv_bytes};
   if (small_supported(M, N, K)) {
     // split-K only while its f32 partial sums stay small (decode-sized batches)
@@ -605,8 +596,7 @@ static int forward_checks(const engram_desc_t* desc, const engram_weights_t* wts
   int rc = gate_checks(desc, x, wts->wkv, wts->q_weight, wts->k_weight, out, M);
   if (rc || M == 0) return rc;
   if (!wts->table || !wts->scales) return fail(ENGRAM_EINVAL, "NULL table");
-  if (!aligned(wts->table, 16) || !aligned(wts->scales, 2))
-    return fail(ENGRAM_EINVAL, "table must be 16-byte aligned, scales 2-byte aligned");
+  if (!aligned(wts->table, 16)) return fail(ENGRAM_EINVAL, "table must be 16-byte aligned");
   if (M >= (int64_t(1) << 31)) return fail(ENGRAM_EINVAL, "B * T too large");
   const int32_t K = n_hash_cols(desc) * desc->head_dim;
   const int32_t N = desc->dim * (desc->hc_mult + 1);
@@ -626,54 +616,6 @@ static int forward_checks(const engram_desc_t* desc, const engram_weights_t* wts
                 "workspace must be 256-byte aligned and >= %zu bytes (%zu for the fastest path)",
                 min_bytes, nplans > 0 ? plans[0].bytes : size_t(0));
   *plan = *best;
-  return ENGRAM_OK;
-}
-
-// The decode step: stages 1-3 in one kernel (hashing `h`'s tokens, or gathering the given `ids`),
-// then the gate from its partial sums; the workspace holds the partial sums and the value rows.
-static int decode_step(const engram_desc_t* desc, const engram_weights_t* wts, const HashArgs& h,
-                       const int32_t* ids, const uint16_t* x, const uint8_t* token_mask,
-                       uint16_t* out, float* gate_out, uint16_t* kv_out, int64_t M,
-                       void* workspace, const LenAdvance& adv, uint32_t* err, cudaStream_t st,
-                       const char* who) {
-  uint8_t* ws = static_cast<uint8_t*>(workspace);
-  DecodeStepArgs a{};
-  a.hash = h;
-  a.ids = ids;
-  a.table = wts->table;
-  a.scales = wts->scales;
-  a.num_rows = desc->num_embeddings;
-  a.w = wts->wkv;
-  a.x = x;
-  a.q = wts->q_weight;
-  a.k = wts->k_weight;
-  a.part = reinterpret_cast<float2*>(ws);
-  a.value = reinterpret_cast<uint16_t*>(ws + round256(decode_step_part_bytes(desc->hc_mult,
-                                                                             desc->dim)));
-  a.kv_out = kv_out;
-  a.M = M;
-  a.N = desc->dim * (desc->hc_mult + 1);
-  a.K = n_hash_cols(desc) * desc->head_dim;
-  a.hc = desc->hc_mult;
-  a.dim = desc->dim;
-  a.err = err;
-  cudaError_t e;
-  if ((e = launch_decode_step(a, st, true)) != cudaSuccess)
-    return cuda_fail(e, who, "decode step");
-  GatePartArgs g{};
-  g.x = x;
-  g.part = a.part;
-  g.value = a.value;
-  g.mask = token_mask;
-  g.out = out;
-  g.gate_out = gate_out;
-  g.M = M;
-  g.hc = desc->hc_mult;
-  g.dim = desc->dim;
-  g.eps = desc->norm_eps;
-  g.inv_sqrt_dim = static_cast<float>(1.0 / std::sqrt(static_cast<double>(desc->dim)));
-  g.adv = adv;
-  if ((e = launch_gate_part(g, st, true)) != cudaSuccess) return cuda_fail(e, who, "gate");
   return ENGRAM_OK;
 }
 
@@ -778,11 +720,6 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   uint16_t* rows = static_cast<uint16_t*>(workspace);   // the projection's input [M, K]
   HashArgs h = make_hash_args(desc, tables, tokens, B, T, cache, cache_len, capacity,
                               hash_ids_out, err);
-  if (plan.path == Path::kDecodeStep) {   // the last kernel advances the cache lengths
-    const LenAdvance adv{cache_len, B, T, capacity};
-    return decode_step(desc, wts, h, nullptr, x, token_mask, out, gate_out, kv_out, M, workspace,
-                       adv, err, st, "engram_forward");
-  }
   HashRowsArgs hr = single_layer_hash_rows(h, wts->table, wts->scales, desc->num_embeddings,
                                            desc->head_dim, rows);
   // 1+2. hash every slot and gather its row into the projection's input, in one kernel. The
@@ -822,14 +759,6 @@ ENGRAM_API int engram_forward_ids(const engram_desc_t* desc, const engram_weight
   uint32_t* err = error_word(&e);
   if (!err) return cuda_fail(e, "engram_forward_ids");
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  if (plan.path == Path::kDecodeStep) {   // stages 2-3 from the given ids, then the gate
-    HashArgs h{};
-    h.n_heads = desc->n_heads;
-    h.max_ngram = desc->max_ngram_size;
-    h.err = err;
-    return decode_step(desc, wts, h, hash_ids, x, token_mask, out, gate_out, kv_out, M,
-                       workspace, LenAdvance{nullptr, 0, 0, 0}, err, st, "engram_forward_ids");
-  }
   // 2. gather and dequantise the rows of every id into the projection's input
   RowsArgs r{};
   r.table = wts->table;

@@ -2,7 +2,6 @@
 // dequantisation (stage 2) and the standalone gate-and-add (stage 4).
 #include "device.cuh"
 #include "hash_rows.cuh"
-#include "decode_step.h"
 #include "kernels.h"
 
 namespace engram {
@@ -327,8 +326,7 @@ __device__ __forceinline__ uint4 gate_out8(uint4 xv, uint4 vv, float g) {
 }
 
 // Block reduction of the three sums; returns the gate (0 for a masked token) to every thread.
-template <class Args>
-__device__ __forceinline__ float block_gate(const Args& a, int64_t m, int32_t s, float sh2,
+__device__ __forceinline__ float block_gate(const GateArgs& a, int64_t m, int32_t s, float sh2,
                                             float sk2, float shwk) {
   __shared__ float red[3][kGateThreads / 32];
   __shared__ float gate_s;
@@ -395,14 +393,23 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
     pdl_wait();
     pdl_launch_dependents();
     advance_lengths(a.adv);
+    // every key and value load is issued before the first is used: the warp issues in order,
+    // so a use between them would wait out each load's latency in turn
+    uint4 kvk[kVec];
 #pragma unroll
     for (int j = 0; j < kVec; ++j) {
       const int v = threadIdx.x + j * kGateThreads;
       if (v < nvec) {
-        const uint4 kv = load_kv8(a, m, N, key0 + 8 * v);
-        if (a.kv_out) reinterpret_cast<uint4*>(a.kv_out + m * N + key0)[v] = kv;
+        kvk[j] = load_kv8(a, m, N, key0 + 8 * v);
         if (keep || write_value) vv[j] = load_kv8(a, m, N, val0 + 8 * v);
-        acc_sums(xv[j], kv, qv[j], kw[j], sh2, sk2, shwk);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+      const int v = threadIdx.x + j * kGateThreads;
+      if (v < nvec) {
+        if (a.kv_out) reinterpret_cast<uint4*>(a.kv_out + m * N + key0)[v] = kvk[j];
+        acc_sums(xv[j], kvk[j], qv[j], kw[j], sh2, sk2, shwk);
       }
     }
     const float g = block_gate(a, m, s, sh2, sk2, shwk);
@@ -438,69 +445,6 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
       reinterpret_cast<uint4*>(orow)[v] = keep ? gate_out8(xv, vv, g) : xv;
     }
   }
-}
-
-// Stage 4 of the decode step: the gate of (token m, stream s) from the projection kernel's
-// partial sums of key^2 and h * w * key (one per 32-column group, added here in group order) and
-// the sum of h^2 over the stream's own x row; then h + gate * value. x and the mask are inputs no
-// kernel of the step writes, so they are loaded before waiting for the projection.
-template <int kVec>
-__global__ void __launch_bounds__(kGateThreads) gate_part_kernel(GatePartArgs a) {
-  const int64_t m = blockIdx.x / a.hc;
-  const int32_t s = blockIdx.x % a.hc;
-  const uint16_t* xr = a.x + (m * a.hc + s) * a.dim;
-  const int nvec = a.dim / 8;
-  const bool keep = a.mask == nullptr || a.mask[m] != 0;
-  uint16_t* orow = a.out + (m * a.hc + s) * a.dim;
-  uint4 xv[kVec];
-  float sh2 = 0.f;
-#pragma unroll
-  for (int j = 0; j < kVec; ++j) {
-    const int v = threadIdx.x + j * kGateThreads;
-    if (v < nvec) {
-      xv[j] = __ldg(reinterpret_cast<const uint4*>(xr) + v);
-      const uint32_t xs[4] = {xv[j].x, xv[j].y, xv[j].z, xv[j].w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float h0 = bf16_bits_to_f32(xs[i] & 0xFFFFu), h1 = bf16_bits_to_f32(xs[i] >> 16);
-        sh2 = fmaf(h0, h0, sh2);
-        sh2 = fmaf(h1, h1, sh2);
-      }
-    }
-  }
-  pdl_wait();
-  pdl_launch_dependents();
-  advance_lengths(a.adv);
-  uint4 vv[kVec];
-#pragma unroll
-  for (int j = 0; j < kVec; ++j) {
-    const int v = threadIdx.x + j * kGateThreads;
-    if (v < nvec && keep) vv[j] = __ldg(reinterpret_cast<const uint4*>(a.value + m * a.dim) + v);
-  }
-  float sk2 = 0.f, shwk = 0.f;
-  const int32_t G = a.dim / 32;
-  for (int32_t t = threadIdx.x; t < G; t += kGateThreads) {
-    const float2 pp = a.part[(static_cast<int64_t>(s) * G + t) * 64 + m];
-    sk2 += pp.x;
-    shwk += pp.y;
-  }
-  const float g = block_gate(a, m, s, sh2, sk2, shwk);
-#pragma unroll
-  for (int j = 0; j < kVec; ++j) {
-    const int v = threadIdx.x + j * kGateThreads;
-    if (v < nvec)   // a masked token's x passes through unchanged
-      reinterpret_cast<uint4*>(orow)[v] = keep ? gate_out8(xv[j], vv[j], g) : xv[j];
-  }
-}
-
-cudaError_t launch_gate_part(const GatePartArgs& a, cudaStream_t st, bool pdl) {
-  const dim3 grid(static_cast<unsigned>(a.M * a.hc)), block(kGateThreads);
-  const int nvec = a.dim / 8;
-  if (nvec <= 1 * kGateThreads) return launch_ex(gate_part_kernel<1>, grid, block, 0, st, pdl, a);
-  if (nvec <= 2 * kGateThreads) return launch_ex(gate_part_kernel<2>, grid, block, 0, st, pdl, a);
-  if (nvec <= 3 * kGateThreads) return launch_ex(gate_part_kernel<3>, grid, block, 0, st, pdl, a);
-  if (nvec <= 4 * kGateThreads) return launch_ex(gate_part_kernel<4>, grid, block, 0, st, pdl, a);
-  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t st, bool pdl) {

@@ -1,12 +1,12 @@
-"""GPU parity of the decode step (up to 64 tokens per call at head_dim 64) against the oracle.
+"""GPU parity of the decode path (up to 64 tokens per call) against the oracle.
 
-At these sizes engram_forward runs one kernel that hashes, gathers and projects inside every CTA,
-then a gate kernel that finishes the gate from that kernel's per-32-column partial sums. The
-cases cover what that kernel does on its own: windows that reach into caches of different
-lengths per sequence (0, 1, 2 and more than max_ngram - 1 entries, so the pad, the cache and
-this call's tokens all feed windows), several tokens of one sequence in one call, token counts
-that are not multiples of 32 (zero rows in the MMA's N), a non-zero pad id, given hash ids, the
-cache append, masks, and the device error bits.
+At these sizes engram_forward hashes and gathers in one kernel, streams the weight over every SM
+in a second (64-row units, a fixed share per SM) and gates in a third. The cases cover what
+decode adds to the prefill tests: windows that reach into caches of different lengths per
+sequence (0, 1, 2 and more than max_ngram - 1 entries, so the pad, the cache and this call's
+tokens all feed windows), several tokens of one sequence in one call, token counts that are not
+multiples of 32 (zero rows in the MMA's N), a non-zero pad id, given hash ids, the cache append,
+masks, and the device error bits.
 """
 import numpy as np
 import pytest
