@@ -33,6 +33,10 @@
  *    device current on its thread). The library's host-side state (the device error word, SM
  *    counts, kernel attributes) is kept per device and guarded; the error word is shared by all
  *    calls on one device.
+ *  - That per-device state (including the device addresses of the error word and of
+ *    engram_forward_noalloc's scratch) is looked up once and kept for the life of the process.
+ *    cudaDeviceReset unloads the library's device code and invalidates it: do not use the
+ *    library on a device after resetting it.
  */
 #ifndef ENGRAM_H_
 #define ENGRAM_H_

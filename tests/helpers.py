@@ -15,7 +15,7 @@ from __future__ import annotations
 import numpy as np
 import torch
 
-from oracle.numerics import bf16_to_f64, bf16_ulp
+from oracle.numerics import bf16_to_f64, bf16_ulp, f64_to_bf16
 
 GATE_ATOL = 2e-4
 OUT_VALUE_RTOL = 2e-4
@@ -79,3 +79,23 @@ def out_violations(out_gpu: np.ndarray, out_ref: np.ndarray, value: np.ndarray) 
 def assert_out_close(out_gpu, out_ref, value):
     bad = out_violations(out_gpu, out_ref, value)
     assert not bad.any(), f"{bad.sum()} outputs beyond tolerance; first {np.argwhere(bad)[:5]}"
+
+
+def kv_flips(kv_gpu: np.ndarray, a: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """Boolean mask of the kv elements where the GPU's bf16 value is not the correctly rounded
+    one, after checking that each of them is a legitimate consequence of f32 accumulation: the
+    GPU's value is the bf16 rounding of a sum within the f32-order bound K 2^-24 sum_k |a_k w_k|
+    of the exact one, i.e. |gpu - exact| <= ulp(gpu) / 2 + that bound. Where the sum does not
+    cancel this is a one-ulp flip at a rounding boundary; where it cancels, the bound (and the
+    flip) can be a few ulps."""
+    A, W = bf16_to_f64(a), bf16_to_f64(w)
+    exact = A @ W.T
+    ref = f64_to_bf16(exact)
+    g = np.asarray(kv_gpu, dtype=np.uint16)
+    flip = g != ref
+    if flip.any():
+        gv = bf16_to_f64(g[flip])
+        bound = a.shape[-1] * 2.0 ** -24 * (np.abs(A) @ np.abs(W).T)[flip]
+        far = np.abs(gv - exact[flip]) > bf16_ulp(gv) / 2 + bound
+        assert not far.any(), f"{far.sum()} kv values not explained by f32 accumulation"
+    return flip

@@ -152,6 +152,13 @@ def test_decode_b64_after_2048_prefill(full):
     np.testing.assert_array_equal(host(length), [P + 2] * B)
 
 
+def whole_tiles(M, tile=256):
+    """Every token of three 256-token tiles of the fused kernel's work: the first, the middle and
+    the last, so that the first, a middle and the last group of its schedule are covered whole."""
+    n = M // tile
+    return np.concatenate([np.arange(t * tile, (t + 1) * tile) for t in (0, n // 2, n - 1)])
+
+
 def _run_large(full, B, T, seed, x_dist, mask_frac, model, want_kv=False):
     batch = synth.make_batch(G, B, T, seed, x_dist=x_dist, mask_frac=mask_frac)
     M = B * T
@@ -186,8 +193,9 @@ def test_masked_b8_t8192_sampled(full):
     np.testing.assert_array_equal(out[~mask], x[~mask])          # every masked token, bit exact
     assert (gate[~mask] == 0).all() and ((gate[mask] > 0) & (gate[mask] < 1)).all()
     rng = np.random.default_rng(5)
-    idx = np.concatenate([rng.choice(np.nonzero(mask)[0], 96, replace=False),
-                          rng.choice(np.nonzero(~mask)[0], 16, replace=False)])
+    idx = np.unique(np.concatenate([rng.choice(np.nonzero(mask)[0], 96, replace=False),
+                                    rng.choice(np.nonzero(~mask)[0], 16, replace=False),
+                                    whole_tiles(M)]))
     check_tokens(dm, ids, x, mask, idx, out, gate)
 
 
@@ -201,6 +209,7 @@ def test_sweep_t65536_sampled(full):
     M = 65536
     batch, ids, out, gate = _run_large(full, 1, M, synth.BASE_SEED + 104, "normal", 0.0,
                                        full.model)
-    idx = np.unique(np.concatenate([[0, M - 1], np.random.default_rng(M).integers(0, M, 64)]))
+    idx = np.unique(np.concatenate([[0, M - 1], np.random.default_rng(M).integers(0, M, 64),
+                                    whole_tiles(M)]))
     check_tokens(full, ids, batch.x.reshape(M, 4, 5120), None, idx, out, gate)
     assert ((gate > 0) & (gate < 1)).all()
