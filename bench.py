@@ -536,7 +536,7 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
     rng = np.random.default_rng(synth.BASE_SEED + 102)
     n = args.warmup + args.steps + 4
     pre = torch.from_numpy(rng.integers(0, geom.vocab, (B, prefill), dtype=np.int32)).cuda()
-    cache = torch.zeros((B, prefill + n + 64), dtype=torch.int32, device="cuda")
+    cache = torch.zeros((B, prefill + 16 * n + 256), dtype=torch.int32, device="cuda")
     cache_len = torch.zeros(B, dtype=torch.int32, device="cuda")
     ids = torch.empty((B, prefill, geom.n_hash_cols), dtype=torch.int32, device="cuda")
     eg.engram_hash(desc, tables, pre, cache, cache_len, ids)
@@ -562,19 +562,45 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
                         "algorithmic_bytes": bytes_step},
            "gpu_launches_per_step": 3, "timing": "CUDA graph replay per step, L2 flushed "
                                                  "(256 MB write) before each"}
-    # The floor a step meets in this setting: one cold read of the 78.6 MB weight by a plain
-    # torch reduction after the same flush. The flush leaves L2 full of dirty lines, so every
-    # line the read brings in also writes one back: the read moves about twice its bytes.
-    wv = weights.wkv.view(torch.float32).view(-1)
-    red = torch.empty((), dtype=torch.float32, device="cuda")
-    floor_ms = time_graph(lambda: torch.sum(wv, dim=0, out=red), flush, args.steps, args.warmup)
-    res["weight_read_floor"] = {
-        "us": round(floor_ms * 1e3, 2),
-        "frac_of_hbm_peak": round(WKV_BYTES / (floor_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
-        "timing": "torch.sum over the wkv weight (78.6 MB, its f32 view flattened), CUDA "
-                  "graph replay, L2 flushed before each as for the steps"}
+    # What the weight stream alone costs in this setting: the step's projection kernel by itself
+    # (engram_wkv on the step's gathered rows: weight stream and kv stores, no hash and no
+    # gate), after the same flush. The flush leaves L2 full of dirty lines, so every line the
+    # stream brings in also writes one back.
+    rows = ws[: B * geom.K * 2].view(torch.int16).view(B, geom.K)
+    kv_alone = torch.empty((B, geom.N), dtype=torch.int16, device="cuda")
+    alone_ms = time_graph(lambda: eg.engram_wkv(rows, weights.wkv, kv_alone), flush, args.steps,
+                          args.warmup)
+    res["projection_alone"] = {
+        "us": round(alone_ms * 1e3, 2),
+        "weight_gbs": round(WKV_BYTES / (alone_ms / 1e3) / 1e9, 1),
+        "frac_of_hbm_peak": round(WKV_BYTES / (alone_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+        "timing": "engram_wkv (the decode projection kernel) alone on the step's rows, CUDA graph "
+                  "replay, L2 flushed before each as for the steps"}
     res["inputs_larger_than_l2"] = decode_rotating(eg, desc, tables, weights, geom, cache,
                                                    cache_len, B, args, peaks, bytes_step)
+    # Stages 2-4 from given hash ids (engram_forward_ids): in a model decode step the hash of
+    # every Engram layer is resolved once (engram_hash_rows_layers or engram_hash) and each layer
+    # then runs only the gather, projection and gate.
+    hid = torch.empty((B, 1, geom.n_hash_cols), dtype=torch.int32, device="cuda")
+    eg.engram_forward(desc, tables, weights, x, tok, cache, cache_len, None, out, ws,
+                      hash_ids_out=hid)
+    x3 = x.view(B, geom.hc_mult, geom.dim)
+    out3 = out.view(B, geom.hc_mult, geom.dim)
+    ids2 = hid.view(B, geom.n_hash_cols)
+    ids_ms = time_graph(lambda: eg.engram_forward_ids(desc, weights, x3, ids2, None, out3, ws),
+                        flush, args.steps, args.warmup)
+    if eg.engram_check_errors() != 0:
+        raise RuntimeError("device error word set during decode from ids")
+    gbs_ids = bytes_step / (ids_ms / 1e3) / 1e9
+    res["from_ids"] = {
+        "workload": f"decode B{B} x 1 token from given hash ids (engram_forward_ids: gather, "
+                    "projection, gate)",
+        "value": round(B / (ids_ms / 1e3), 1), "unit": "tokens/s",
+        "us_per_step": round(ids_ms * 1e3, 2),
+        "roofline": {"bound": "hbm", "achieved": round(gbs_ids, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs_ids / peaks["hbm_gbs"], 4),
+                     "algorithmic_bytes": bytes_step},
+        "timing": "CUDA graph replay per step, L2 flushed (256 MB write) before each"}
     if in_graph_ms is not None:
         # the same steps without a graph launch per step: what a serving loop that captures many
         # layers or steps in one graph sees
