@@ -536,30 +536,37 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         }
       }
 
+      const int32_t s = it.col / nk;                 // key item: its stream
+      // w = q * k of the key tile's 256 columns (a product of two bf16 values, exact in f32):
+      // lane l forms those of columns 8 l .. 8 l + 7 from one 16-byte load of q and one of k,
+      // issued before the accumulator wait; each box then takes its 32 columns from the lanes
+      // that hold them by broadcast shuffles
+      float w8[8];
+      if (!it.value) {
+        const int64_t q0 = static_cast<int64_t>(s) * dim + (it.col % nk) * kBN + 8 * lane;
+        const uint4 qa = __ldg(reinterpret_cast<const uint4*>(p.q + q0));
+        const uint4 ka = __ldg(reinterpret_cast<const uint4*>(p.k + q0));
+        const uint32_t qw[4] = {qa.x, qa.y, qa.z, qa.w}, kw[4] = {ka.x, ka.y, ka.z, ka.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          w8[2 * e] = lo_bf16(qw[e]) * lo_bf16(kw[e]);
+          w8[2 * e + 1] = hi_bf16(qw[e]) * hi_bf16(kw[e]);
+        }
+      }
+
       const uint32_t acc = t_all & 1, acc_phase = (t_all >> 1) & 1;
       ok = mbar_wait(&sh->tfull[acc], acc_phase, abort, p.err);
       ok = __all_sync(0xFFFFFFFFu, ok);
       if (ok) tc_fence_after();
       const uint32_t tbase = tmem_base + lane_base + acc * kBN + half * 32;
       float sh2[2] = {0.f, 0.f}, sk2[2] = {0.f, 0.f}, shwk[2] = {0.f, 0.f};
-      const int32_t s = it.col / nk;                 // key item: its stream
       if (!it.value) {
         // key tile: columns d0 .. d0 + 255 of stream s, in four 64-column boxes
         for (int c4 = 0; c4 < kBN / kXCols && ok; ++c4) {
           const int32_t d = (it.col % nk) * kBN + c4 * kXCols + half * 32;   // this half's columns
+          const int src0 = (c4 * kXCols + half * 32) / 8;   // lane holding the box-half's column 0
           uint32_t r[32];
           tc_ld_32x32b_x32(tbase + c4 * kXCols, r);
-          // w = q * k for these 32 columns: the same for every lane (a product of two bf16
-          // values, exact in f32)
-          uint32_t qv[16], kv[16];
-          const uint4* qp = reinterpret_cast<const uint4*>(p.q + static_cast<int64_t>(s) * dim + d);
-          const uint4* kp = reinterpret_cast<const uint4*>(p.k + static_cast<int64_t>(s) * dim + d);
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            const uint4 a = __ldg(qp + j), b = __ldg(kp + j);
-            qv[4 * j] = a.x; qv[4 * j + 1] = a.y; qv[4 * j + 2] = a.z; qv[4 * j + 3] = a.w;
-            kv[4 * j] = b.x; kv[4 * j + 1] = b.y; kv[4 * j + 2] = b.z; kv[4 * j + 3] = b.w;
-          }
           ok = mbar_wait(&sh->xfull[xr.slot], xr.phase, abort, p.err);
           ok = __all_sync(0xFFFFFFFFu, ok);
           uint32_t xv[16];
@@ -571,8 +578,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
 #pragma unroll
           for (int e = 0; e < 16; ++e) {
             kb16[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
-            const float w0 = lo_bf16(qv[e]) * lo_bf16(kv[e]);
-            const float w1 = hi_bf16(qv[e]) * hi_bf16(kv[e]);
+            const float w0 = __shfl_sync(0xFFFFFFFFu, w8[(2 * e) % 8], src0 + (2 * e) / 8);
+            const float w1 = __shfl_sync(0xFFFFFFFFu, w8[(2 * e + 1) % 8], src0 + (2 * e + 1) / 8);
             const float key0 = lo_bf16(kb16[e]), key1 = hi_bf16(kb16[e]);
             const float h0 = lo_bf16(xv[e]), h1 = hi_bf16(xv[e]);
             sh2[0] = fmaf(h0, h0, sh2[0]);
