@@ -168,14 +168,24 @@ constexpr size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 //  - kUnfused: the persistent projection GEMM into a bf16 kv, then the gate kernel; measured
 //              faster than the fused kernel below 640 tokens (too few items to fill the GPU
 //              past the fused kernel's cold start: 72 vs 74 us at 512, 86 vs 82 us at 640);
+//  - kFusedDeferred: 512 to 2048 tokens: the fused kernel with deferred output: its value
+//              tiles store bf16 value rows instead of waiting for the gates, and a light kernel
+//              then writes out = x + gate * value; for batches too small for the fused kernel to
+//              hide its value tiles' wait and x traffic behind the key tiles of other token
+//              tiles;
 //  - kFused:   projection + gate in one kernel; kv never touches HBM; least workspace.
-enum class Path { kDecode, kSmall, kUnfused, kFused };
+enum class Path { kDecode, kSmall, kUnfused, kFusedDeferred, kFused };
 struct Plan {
   Path path;
   int ksplit;
   size_t bytes;
 };
 constexpr int64_t kFusedMinTokens = 640;
+// the deferred-output fused plan's range, measured on one GPU against the other plans (A/B):
+// 65.6 vs 70.0 us at 512 tokens, 96.7 vs 105.3 at 1024, 150.8 vs 157.6 at 2048; slower at 384
+// (63.8 vs 58.0) and at 4096 (281 vs 266)
+constexpr int64_t kDeferredMinTokens = 512;
+constexpr int64_t kDeferredMaxTokens = 2048;
 constexpr int kMaxPlans = 6;
 
 // Candidate plans in order of preference; returns how many were written.
@@ -188,6 +198,10 @@ int forward_plans(const engram_desc_t* d, int64_t M, Plan* out) {
   const bool fused = fused_supported(K, d->hc_mult, d->dim);
   int n = 0;
   if (decode_supported(M, N, K)) out[n++] = {Path::kDecode, 1, base + kv_bytes};
+  if (fused && M >= kDeferredMinTokens && M <= kDeferredMaxTokens)
+    out[n++] = {Path::kFusedDeferred, 1,
+                base + round256(fused_scratch_bytes(M, d->hc_mult, d->dim)) +
+                    round256(size_t(M) * d->dim * 2)};
   if (small_supported(M, N, K)) {
     // split-K only while its f32 partial sums stay small (decode-sized batches)
     const int ks = M <= 64 ? small_ksplit(N, K) : 1;
@@ -633,14 +647,30 @@ static int project_and_gate(const engram_desc_t* desc, const Plan& plan,
   const uint16_t* rows = static_cast<const uint16_t*>(workspace);
   uint8_t* ws = static_cast<uint8_t*>(workspace) + round256(size_t(M) * K * 2);
   cudaError_t e;
-  if (plan.path == Path::kFused) {
+  if (plan.path == Path::kFused || plan.path == Path::kFusedDeferred) {
     // 3+4. projection with the gate fused into its epilogue
     FusedArgs f = make_fused_args(desc, rows, wts->wkv, x, wts->q_weight, wts->k_weight,
                                   token_mask, out, gate_out, kv_out, M, err);
     f.adv = adv;
     f.scratch = ws;
     f.sync_cleared = true;
+    if (plan.path == Path::kFusedDeferred)   // value rows after the fused kernel's scratch
+      f.vout = reinterpret_cast<uint16_t*>(ws + round256(fused_scratch_bytes(M, desc->hc_mult,
+                                                                              desc->dim)));
     if ((e = launch_fused(f, st, true)) != cudaSuccess) return cuda_fail(e, who, "fused");
+    if (plan.path == Path::kFusedDeferred) {
+      GateApplyArgs g{};
+      g.x = x;
+      g.gx = fused_gates(ws);
+      g.value = f.vout;
+      g.mask = token_mask;
+      g.out = out;
+      g.M = M;
+      g.hc = desc->hc_mult;
+      g.dim = desc->dim;
+      if ((e = launch_gate_apply(g, st, true)) != cudaSuccess)
+        return cuda_fail(e, who, "gate apply");
+    }
     return ENGRAM_OK;
   }
   // 3. projection -> bf16 kv (or f32 split-K partials); 4. gate and add
@@ -726,7 +756,8 @@ ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* 
   // kernels of the chain are launched with programmatic stream serialization: each overlaps its
   // launch and prologue with the previous one and waits for it before touching its data.
   const int32_t K = n_hash_cols(desc) * desc->head_dim;
-  if (plan.path == Path::kFused)   // the fused kernel's counters, cleared by the hash kernel
+  // the fused kernel's counters, cleared by the hash kernel
+  if (plan.path == Path::kFused || plan.path == Path::kFusedDeferred)
     fused_sync_region(static_cast<uint8_t*>(workspace) + round256(size_t(M) * K * 2), M,
                       desc->hc_mult, desc->dim, &hr.zero, &hr.zero_n);
   if ((e = launch_hash_rows(hr, st, true)) != cudaSuccess)
@@ -769,7 +800,8 @@ ENGRAM_API int engram_forward_ids(const engram_desc_t* desc, const engram_weight
   r.head_dim = desc->head_dim;
   r.out = static_cast<uint16_t*>(workspace);
   r.err = err;
-  if (plan.path == Path::kFused)   // the fused kernel's counters, cleared by the rows kernel
+  // the fused kernel's counters, cleared by the rows kernel
+  if (plan.path == Path::kFused || plan.path == Path::kFusedDeferred)
     fused_sync_region(static_cast<uint8_t*>(workspace) + round256(size_t(M) * K * 2), M,
                       desc->hc_mult, desc->dim, &r.zero, &r.zero_n);
   if ((e = launch_rows(r, st, true)) != cudaSuccess)

@@ -98,6 +98,7 @@ struct FusedParams {
   uint16_t* out;
   float* gate_out;
   uint16_t* kv_out;
+  uint16_t* vout;     // [M, dim] value rows (deferred output), or null
   float* gx;          // [M, hc] gates, exchanged between pairs
   float* part;        // [m_tiles, 2, hc, nk, 3, 128] per-key-tile partial sums
   int32_t* next;      // item counter; zero at launch
@@ -416,7 +417,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         if (idx < 0) break;
         const FusedItem it = fused_item_at(sched, idx);
         const int32_t m0 = it.mt * kTokensPerTile + half_m * kBM;
-        const int steps = it.value ? (kBN / kXCols) * hc : kBN / kXCols;
+        // (deferred output: a value item reads no x)
+        const int steps = it.value ? (p.vout ? 0 : (kBN / kXCols) * hc) : kBN / kXCols;
         for (int q = 0; q < steps; ++q) {
           int32_t col, stream;
           if (it.value) {
@@ -524,7 +526,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
       float gl[kMaxHc];
 #pragma unroll
       for (int i = 0; i < kMaxHc; ++i) gl[i] = 0.f;
-      if (it.value) {
+      if (it.value && p.vout == nullptr) {
         // the gates of every stream of these tokens (bounded wait)
         bool got = true;
         if (threadIdx.x == 64) got = wait_flags(fl, hc, abort, p.err);
@@ -591,6 +593,24 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
           }
           if (valid && p.kv_out)
             store_words<16>(p.kv_out + m * N + static_cast<int64_t>(s) * dim + d, kb16);
+        }
+      } else if (p.vout != nullptr) {
+        // value tile, deferred output: the bf16 value rows only; a later kernel adds
+        // gate * value to x once every gate exists, so this item waits for no key tile
+        const int32_t col0 = it.col * kBN;
+        for (int c4 = 0; c4 < kBN / kXCols && ok; ++c4) {
+          const int32_t colb = col0 + c4 * kXCols + half * 32;
+          uint32_t r[32];
+          tc_ld_32x32b_x32(tbase + c4 * kXCols, r);
+          tc_wait_ld(r);
+          uint32_t vb[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e)
+            vb[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
+          if (valid) {
+            store_words<16>(p.vout + m * dim + colb, vb);
+            if (p.kv_out) store_words<16>(p.kv_out + m * N + static_cast<int64_t>(hc) * dim + colb, vb);
+          }
         }
       } else {
         // value tile: value columns col0 .. col0 + 255, shared by all hc streams. Each (64-column
@@ -745,6 +765,10 @@ size_t fused_scratch_bytes(int64_t M, int32_t hc, int32_t dim) {
   return scratch_layout(M, hc, dim).total;
 }
 
+const float* fused_gates(const void* scratch) {
+  return reinterpret_cast<const float*>(static_cast<const uint8_t*>(scratch));   // layout: gx first
+}
+
 void fused_sync_region(void* scratch, int64_t M, int32_t hc, int32_t dim, int32_t** ptr,
                        int32_t* count) {
   const ScratchLayout l = scratch_layout(M, hc, dim);
@@ -786,6 +810,7 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl) {
   p.out = a.out;
   p.gate_out = a.gate_out;
   p.kv_out = a.kv_out;
+  p.vout = a.vout;
   p.gx = reinterpret_cast<float*>(base + l.gx);
   p.part = reinterpret_cast<float*>(base + l.part);
   p.next = sync;

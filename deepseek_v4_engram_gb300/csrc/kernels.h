@@ -139,6 +139,20 @@ struct FusedArgs {
   LenAdvance adv;         // adv.len may be null
   void* scratch;          // fused_scratch_bytes(M, hc, dim) bytes, 256-byte aligned
   bool sync_cleared;      // the scratch's counters were cleared by the previous kernel
+  uint16_t* vout;         // [M, dim] or null. Set: deferred output: value tiles store their bf16
+                          // value rows here and do not write out (launch_gate_apply does, after)
+};
+
+// out = h + gate * value from the gates and value rows the fused kernel left in its deferred
+// output mode: one block per (token, stream).
+struct GateApplyArgs {
+  const uint16_t* x;      // [M, hc, dim]
+  const float* gx;        // [M, hc] gates (0 for a masked token)
+  const uint16_t* value;  // [M, dim] bf16
+  const uint8_t* mask;    // [M] or null
+  uint16_t* out;          // [M, hc, dim]
+  int64_t M;
+  int32_t hc, dim;
 };
 
 // The counters in the fused kernel's scratch that must be zero when it starts.
@@ -162,6 +176,9 @@ bool decode_supported(int64_t M, int32_t N, int32_t K);
 cudaError_t launch_wkv_decode(const WkvSmallArgs& a, cudaStream_t s, bool pdl = false);
 bool fused_supported(int32_t K, int32_t hc, int32_t dim);
 size_t fused_scratch_bytes(int64_t M, int32_t hc, int32_t dim);
+// The gates [M, hc] f32 at the start of the fused kernel's scratch.
+const float* fused_gates(const void* scratch);
+cudaError_t launch_gate_apply(const GateApplyArgs& a, cudaStream_t s, bool pdl = false);
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s, bool pdl = false);
 
 // cudaLaunchKernelEx with optional programmatic stream serialization.

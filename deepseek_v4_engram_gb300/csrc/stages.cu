@@ -447,6 +447,49 @@ __global__ void __launch_bounds__(kGateThreads) gate_kernel(GateArgs a) {
   }
 }
 
+// out = h + gate * value for (token m, stream s) from the fused kernel's deferred output: its gates
+// and bf16 value rows. x and the mask are inputs no kernel of the forward writes, so they are
+// loaded before waiting for the fused kernel.
+template <int kVec>
+__global__ void __launch_bounds__(kGateThreads) gate_apply_kernel(GateApplyArgs a) {
+  const int64_t m = blockIdx.x / a.hc;
+  const int32_t s = blockIdx.x % a.hc;
+  const uint16_t* xr = a.x + (m * a.hc + s) * a.dim;
+  const int nvec = a.dim / 8;
+  const bool keep = a.mask == nullptr || a.mask[m] != 0;
+  uint16_t* orow = a.out + (m * a.hc + s) * a.dim;
+  uint4 xv[kVec], vv[kVec];
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    const int v = threadIdx.x + j * kGateThreads;
+    if (v < nvec) xv[j] = __ldg(reinterpret_cast<const uint4*>(xr) + v);
+  }
+  pdl_wait();
+  pdl_launch_dependents();
+  const float g = keep ? a.gx[m * a.hc + s] : 0.f;
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    const int v = threadIdx.x + j * kGateThreads;
+    if (v < nvec && keep) vv[j] = __ldg(reinterpret_cast<const uint4*>(a.value + m * a.dim) + v);
+  }
+#pragma unroll
+  for (int j = 0; j < kVec; ++j) {
+    const int v = threadIdx.x + j * kGateThreads;
+    if (v < nvec)   // a masked token's x passes through unchanged
+      reinterpret_cast<uint4*>(orow)[v] = keep ? gate_out8(xv[j], vv[j], g) : xv[j];
+  }
+}
+
+cudaError_t launch_gate_apply(const GateApplyArgs& a, cudaStream_t st, bool pdl) {
+  const dim3 grid(static_cast<unsigned>(a.M * a.hc)), block(kGateThreads);
+  const int nvec = a.dim / 8;
+  if (nvec <= 1 * kGateThreads) return launch_ex(gate_apply_kernel<1>, grid, block, 0, st, pdl, a);
+  if (nvec <= 2 * kGateThreads) return launch_ex(gate_apply_kernel<2>, grid, block, 0, st, pdl, a);
+  if (nvec <= 3 * kGateThreads) return launch_ex(gate_apply_kernel<3>, grid, block, 0, st, pdl, a);
+  if (nvec <= 4 * kGateThreads) return launch_ex(gate_apply_kernel<4>, grid, block, 0, st, pdl, a);
+  return cudaErrorInvalidValue;
+}
+
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t st, bool pdl) {
   const dim3 grid(static_cast<unsigned>(a.M * a.hc)), block(kGateThreads);
   const int nvec = a.dim / 8;

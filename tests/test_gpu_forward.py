@@ -156,6 +156,19 @@ def test_forward_full_width(wide, B, T, mask_frac, ws_mode):
     check_against_oracle(wide, batch, run_forward(wide, batch, ws_mode=ws_mode))
 
 
+@pytest.mark.parametrize("B,T", [(1, 512), (1, 700), (2, 1024)])
+def test_deferred_output_equals_fused(wide, B, T):
+    # from 512 to 2048 tokens the fastest workspace runs the fused kernel with its output deferred
+    # (bf16 value rows, then out = x + gate * value in a second kernel); the minimum workspace runs
+    # the fused kernel alone. Both round the value to bf16 and take one fma per element: equal bits.
+    batch = synth.make_batch(wide.geom, B, T, synth.BASE_SEED + 260 + T, x_dist="student_t3",
+                             mask_frac=0.1)
+    deferred = run_forward(wide, batch, ws_mode="fastest")
+    fused = run_forward(wide, batch, ws_mode="min")
+    for key in ("out", "gate", "kv", "hash_ids"):
+        np.testing.assert_array_equal(deferred[key], fused[key])
+
+
 def test_prefill_then_decode_equals_one_prefill(wide):
     # the look-back cache carries across calls: prefill(T) == prefill(T-j) + j decode steps
     B, T, j = 3, 40, 4

@@ -72,7 +72,8 @@ def run(dm, batch, noalloc: bool):
 # (model, B, T, path engram_forward_noalloc takes at that size)
 CALLS = [("wide", 64, 1, "fastest"),     # decode: weight-streaming projection, bf16 kv (~3.5 MB)
          ("tiny", 2, 150, "fastest"),    # 300 tokens at dim 256: projection GEMM, then the gate
-         ("wide", 1, 1024, "fastest"),   # the fused projection + gate kernel
+         ("wide", 2, 256, "fastest"),    # 512 tokens: fused kernel, deferred output (~7.4 MB)
+         ("wide", 1, 1024, "fused"),     # its deferred-output plan needs ~14.6 MB: the fused one
          ("wide", 3, 77, "fused")]       # its fastest path needs ~12.5 MB: the fused one fits
 
 
