@@ -151,6 +151,15 @@ def engram_embed_rows(desc, table, scales, ids, out, stream=None):
                                    ids.numel(), _ptr(out, "bf16", "out"), _stream(stream)))
 
 
+def engram_embed_rows_shard(desc, table_shard, scales_shard, row_begin: int, ids, out,
+                            stream=None):
+    shard_rows = 0 if table_shard is None else table_shard.shape[0]
+    _check(lib().engram_embed_rows_shard(ctypes.byref(desc), _ptr(table_shard, "u8", "table_shard"),
+                                         _ptr(scales_shard, "u8", "scales_shard"), row_begin,
+                                         shard_rows, _ptr(ids, "i32", "ids"), ids.numel(),
+                                         _ptr(out, "bf16", "out"), _stream(stream)))
+
+
 def engram_wkv(a, w, kv, stream=None):
     M, K = a.shape
     N = w.shape[0]

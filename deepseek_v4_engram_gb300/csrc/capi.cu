@@ -10,6 +10,7 @@
 
 #include "engram.h"
 #include "kernels.h"
+#include "shard.h"
 
 namespace engram {
 
@@ -453,6 +454,40 @@ ENGRAM_API int engram_embed_rows(const engram_desc_t* desc, const uint8_t* table
   r.err = err;
   if ((e = launch_rows(r, static_cast<cudaStream_t>(stream))) != cudaSuccess)
     return cuda_fail(e, "engram_embed_rows");
+  return ENGRAM_OK;
+}
+
+ENGRAM_API int engram_embed_rows_shard(const engram_desc_t* desc, const uint8_t* table_shard,
+                                       const uint8_t* scales_shard, int64_t row_begin,
+                                       int64_t shard_rows, const int32_t* ids, int64_t n_ids,
+                                       uint16_t* out, void* stream) {
+  g_msg[0] = 0;
+  int rc = check_desc(desc);
+  if (rc) return rc;
+  if (n_ids < 0 || n_ids >= (int64_t(1) << 36)) return fail(ENGRAM_EINVAL, "bad n_ids");
+  if (row_begin < 0 || shard_rows < 0 || row_begin + shard_rows > desc->num_embeddings)
+    return fail(ENGRAM_EINVAL, "the shard's rows must lie in [0, num_embeddings)");
+  if (n_ids == 0) return ENGRAM_OK;
+  if (!ids || !out || (shard_rows > 0 && (!table_shard || !scales_shard)))
+    return fail(ENGRAM_EINVAL, "NULL array");
+  if ((shard_rows > 0 && !aligned(table_shard, 16)) || !aligned(out, 16) || !aligned(ids, 4))
+    return fail(ENGRAM_EINVAL, "table_shard and out must be 16-byte aligned, ids 4-byte aligned");
+  cudaError_t e;
+  uint32_t* err = error_word(&e);
+  if (!err) return cuda_fail(e, "engram_embed_rows_shard");
+  ShardRowsArgs r{};
+  r.table = table_shard;
+  r.scales = scales_shard;
+  r.ids = ids;
+  r.n_ids = n_ids;
+  r.row_begin = row_begin;
+  r.shard_rows = shard_rows;
+  r.num_rows = desc->num_embeddings;
+  r.head_dim = desc->head_dim;
+  r.out = out;
+  r.err = err;
+  if ((e = launch_shard_rows(r, static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return cuda_fail(e, "engram_embed_rows_shard");
   return ENGRAM_OK;
 }
 

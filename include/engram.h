@@ -189,6 +189,26 @@ ENGRAM_API int engram_embed_rows(const engram_desc_t* desc, const uint8_t* table
                                  uint16_t* out, void* stream);
 
 /*
+ * Stage 2 over a row-sharded table (Engram listing, __init__: the embedding is a
+ * ParallelEngramEmbedding; the pages do not say how it splits the table: this library reads it
+ * as contiguous ranges of rows, one per rank). The calling rank holds rows
+ * [row_begin, row_begin + shard_rows) of the num_embeddings-row table:
+ *   table_shard uint8 e4m3fn [shard_rows, head_dim] (16-byte aligned), scales_shard uint8 e8m0
+ *   [shard_rows, head_dim / 32]; ids int32 [n_ids] GLOBAL row ids; out bf16 [n_ids, head_dim].
+ * A row the rank holds is written as engram_embed_rows writes it; a row in [0, num_embeddings)
+ * that another rank holds is written as bf16 -0.0 in every element. -0 is the identity of IEEE
+ * addition, so the element-wise bf16 sum of every rank's out (an all-reduce, in any order) equals
+ * engram_embed_rows over the whole table bit for bit, signed zeros included. An id outside
+ * [0, num_embeddings) writes a zero row and sets ENGRAM_DEVERR_ID_RANGE (on every rank).
+ * A shard outside [0, num_embeddings) returns ENGRAM_EINVAL; shard_rows = 0 (a rank with no rows)
+ * writes -0 rows only. The exchange itself is the caller's (one all-reduce of out).
+ */
+ENGRAM_API int engram_embed_rows_shard(const engram_desc_t* desc, const uint8_t* table_shard,
+                                       const uint8_t* scales_shard, int64_t row_begin,
+                                       int64_t shard_rows, const int32_t* ids, int64_t n_ids,
+                                       uint16_t* out, void* stream);
+
+/*
  * Stage 3, the wkv projection (page "Module engram", stage 3 and function linear_bf16; Engram
  * listing, forward: self.wkv(...)). kv[m, n] = bf16(sum_k a[m, k] * w[n, k]), f32 accumulation
  * on the tensor cores, one rounding to bf16.

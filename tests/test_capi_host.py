@@ -60,6 +60,20 @@ def test_desc_validation(lib, bad):
     assert lib.engram_forward_workspace_size(ctypes.byref(d), 16) == 0
 
 
+def test_shard_rows_validation(lib):
+    d = desc()
+    n = d.num_embeddings
+    f = lib.engram_embed_rows_shard
+    # the shard must lie in [0, num_embeddings)
+    assert f(ctypes.byref(d), 16, 16, -1, 10, 16, 4, 16, None) == _lib.ENGRAM_EINVAL
+    assert f(ctypes.byref(d), 16, 16, n - 5, 10, 16, 4, 16, None) == _lib.ENGRAM_EINVAL
+    assert b"shard" in lib.engram_last_error()
+    # NULL ids, a misaligned shard; nothing to do for 0 ids
+    assert f(ctypes.byref(d), 16, 16, 0, 10, None, 4, 16, None) == _lib.ENGRAM_EINVAL
+    assert f(ctypes.byref(d), 24, 16, 0, 10, 16, 4, 16, None) == _lib.ENGRAM_EINVAL
+    assert f(ctypes.byref(d), None, None, 0, 0, None, 0, None, None) == _lib.ENGRAM_OK
+
+
 def test_gate_rejects_aliasing_and_misalignment(lib):
     d = desc()
     x = 0x10000
