@@ -413,8 +413,10 @@ def run_configs(eg, desc, tables, weights, model, geom, flush, peaks):
     tmax = max(w["T_list"])
     tok_all = dev(synth.make_tokens(geom, 1, tmax, np.random.default_rng(w["batch_seed"])))
     x_all = synth.make_x_device((1, tmax, geom.hc_mult, geom.dim), w["batch_seed"])
-    sweep = []
-    for T in w["T_list"]:
+    sweep, between = [], []
+    # the configured points, then the plan boundaries between them (256: small-batch projection;
+    # 1024, 2048: fused kernel with deferred output)
+    for T in tuple(w["T_list"]) + (256, 1024, 2048):
         steps = 20 if T <= 4096 else 5
         small = T <= 512   # where the graph launch per step is a visible share of the step
         r = time_forward(eg, desc, tables, weights, x_all[:, :T].contiguous(),
@@ -427,12 +429,12 @@ def run_configs(eg, desc, tables, weights, model, geom, flush, peaks):
         if ms_graph is not None:
             point["in_graph"] = {"us_per_step": round(ms_graph * 1e3, 2),
                                  "roofline_frac": round(roofline_of(T, ms_graph, peaks)[1], 4)}
-        sweep.append(point)
+        (sweep if T in w["T_list"] else between).append(point)
     res["layers"] = run_layers(eg, desc, tables, geom, flush, peaks)
     res["layers"]["workload"] = ("stages 1+2 for 4 Engram layers (own constants and tables), one "
                                  "launch vs one call per layer")
     res["sweep"] = {"workload": "prefill B1, T = 1 .. 65536", "unit": "tokens/s",
-                    "points": sweep,
+                    "points": sweep, "between": between,
                     "in_graph_timing": "T <= 512: also 8 steps in one CUDA graph, L2 flushed "
                                        "before each, event record nodes around each step",
                     "crossover_tokens": round(WKV_BYTES / (FLOPS_PER_TOKEN / (peaks["bf16_tflops"]
@@ -576,6 +578,22 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
         "frac_of_hbm_peak": round(WKV_BYTES / (alone_ms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
         "timing": "engram_wkv (the decode projection kernel) alone on the step's rows, CUDA graph "
                   "replay, L2 flushed before each as for the steps"}
+    # The floor under that: one read of the weight over every SM that does nothing with the bytes
+    # (engram_probe_stream_read: bulk copies into the projection's ring depth, or plain loads),
+    # after the same flush.
+    floor = {}
+    for method, name in ((0, "bulk_copies"), (1, "plain_loads")):
+        f_ms = time_graph(lambda m=method: eg.api.engram_probe_stream_read(weights.wkv, m), flush,
+                          args.steps, args.warmup)
+        floor[name] = {"us": round(f_ms * 1e3, 2),
+                       "gbs": round(WKV_BYTES / (f_ms / 1e3) / 1e9, 1),
+                       "frac_of_hbm_peak": round(WKV_BYTES / (f_ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                                                 4)}
+    floor["timing"] = ("engram_probe_stream_read over the 78.6 MB wkv weight, CUDA graph replay, "
+                       "L2 flushed before each as for the steps")
+    res["stream_floor"] = floor
+    if eg.engram_check_errors() != 0:
+        raise RuntimeError("device error word set by the stream probe")
     res["inputs_larger_than_l2"] = decode_rotating(eg, desc, tables, weights, geom, cache,
                                                    cache_len, B, args, peaks, bytes_step)
     # Stages 2-4 from given hash ids (engram_forward_ids): in a model decode step the hash of

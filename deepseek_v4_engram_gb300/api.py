@@ -160,6 +160,15 @@ def engram_embed_rows_shard(desc, table_shard, scales_shard, row_begin: int, ids
                                          _ptr(out, "bf16", "out"), _stream(stream)))
 
 
+def engram_probe_stream_read(buf, method: int, stream=None):
+    """One read of `buf` (a contiguous CUDA tensor) over every SM: 0 bulk copies, 1 plain loads."""
+    if not (isinstance(buf, torch.Tensor) and buf.is_cuda and buf.is_contiguous()):
+        raise TypeError("buf: expected a contiguous CUDA tensor")
+    _check(lib().engram_probe_stream_read(ctypes.c_void_p(buf.data_ptr()),
+                                          buf.numel() * buf.element_size(), method,
+                                          _stream(stream)))
+
+
 def engram_wkv(a, w, kv, stream=None):
     M, K = a.shape
     N = w.shape[0]

@@ -11,6 +11,7 @@
 #include "engram.h"
 #include "kernels.h"
 #include "shard.h"
+#include "stream_probe.h"
 
 namespace engram {
 
@@ -488,6 +489,23 @@ ENGRAM_API int engram_embed_rows_shard(const engram_desc_t* desc, const uint8_t*
   r.err = err;
   if ((e = launch_shard_rows(r, static_cast<cudaStream_t>(stream))) != cudaSuccess)
     return cuda_fail(e, "engram_embed_rows_shard");
+  return ENGRAM_OK;
+}
+
+ENGRAM_API int engram_probe_stream_read(const void* src, size_t bytes, int32_t method,
+                                        void* stream) {
+  g_msg[0] = 0;
+  if (method != kProbeBulk && method != kProbePlain) return fail(ENGRAM_EINVAL, "bad method");
+  if (bytes % 16 != 0 || bytes >= (size_t(1) << 40))
+    return fail(ENGRAM_EINVAL, "bytes must be a multiple of 16 below 2^40");
+  if (bytes == 0) return ENGRAM_OK;
+  if (!src || !aligned(src, 16)) return fail(ENGRAM_EINVAL, "src must be 16-byte aligned");
+  cudaError_t e;
+  uint32_t* err = error_word(&e);
+  if (!err) return cuda_fail(e, "engram_probe_stream_read");
+  if ((e = launch_stream_probe(src, static_cast<int64_t>(bytes), method, err,
+                               static_cast<cudaStream_t>(stream))) != cudaSuccess)
+    return cuda_fail(e, "engram_probe_stream_read");
   return ENGRAM_OK;
 }
 

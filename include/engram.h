@@ -371,6 +371,20 @@ ENGRAM_API int engram_forward_noalloc(const engram_desc_t* desc, const engram_ta
                                       int32_t* hash_ids_out, float* gate_out, uint16_t* kv_out,
                                       void* stream);
 
+/*
+ * A measurement call, not a stage of the forward (it has no counterpart on the pages): one read of
+ * the device buffer src[0, bytes) spread evenly over every SM, discarding the bytes. Its duration
+ * bounds from below any kernel that streams the same buffer once from the same memory state (the
+ * decode projection streams the wkv weight once per step), whatever that kernel computes.
+ *   method 0: 32 KB bulk copies (cp.async.bulk) into a 6-stage shared-memory ring per SM (the
+ *             decode projection's bytes in flight); method 1: 16-byte non-caching loads, 512
+ *             threads per SM, four loads in flight per thread.
+ * src must be 16-byte aligned and bytes a multiple of 16 (else ENGRAM_EINVAL); bytes = 0 launches
+ * nothing. Writes nothing the caller can see.
+ */
+ENGRAM_API int engram_probe_stream_read(const void* src, size_t bytes, int32_t method,
+                                        void* stream);
+
 #ifdef __cplusplus
 }
 #endif

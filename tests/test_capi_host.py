@@ -74,6 +74,15 @@ def test_shard_rows_validation(lib):
     assert f(ctypes.byref(d), None, None, 0, 0, None, 0, None, None) == _lib.ENGRAM_OK
 
 
+def test_stream_probe_validation(lib):
+    f = lib.engram_probe_stream_read
+    assert f(16, 64, 2, None) == _lib.ENGRAM_EINVAL            # no such method
+    assert f(16, 40, 0, None) == _lib.ENGRAM_EINVAL            # not a multiple of 16 bytes
+    assert f(24, 64, 1, None) == _lib.ENGRAM_EINVAL            # misaligned
+    assert f(None, 64, 0, None) == _lib.ENGRAM_EINVAL
+    assert f(None, 0, 0, None) == _lib.ENGRAM_OK               # nothing to read
+
+
 def test_gate_rejects_aliasing_and_misalignment(lib):
     d = desc()
     x = 0x10000

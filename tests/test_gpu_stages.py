@@ -217,3 +217,13 @@ def test_gate_zero_key_and_tiny(tiny):
     np.testing.assert_allclose(host(gate)[:4], 1 / (1 + np.exp(-1e-3)), atol=1e-6)
     assert_gate_close(host(gate), ref_gate)
     assert_out_close(host(out), ref_out, kv[:, g.hc_mult * g.dim:])
+
+
+@pytest.mark.parametrize("nbytes", [16, 48 * 1024 + 16, 78643200])
+def test_stream_probe_reads_without_error(nbytes):
+    # the measurement call: every share of the buffer read, every wait completed in time
+    buf = torch.empty(nbytes // 4, dtype=torch.int32, device="cuda").fill_(7)
+    for method in (0, 1):
+        eg.api.engram_probe_stream_read(buf, method)
+    torch.cuda.synchronize()
+    assert eg.engram_check_errors() == 0
