@@ -357,7 +357,7 @@ ENGRAM_API int engram_forward_ids(const engram_desc_t* desc, const engram_weight
  *
  * This call allocates nothing: no cudaMalloc, no cudaFree, no allocating library routine. Its
  * first call on a device looks up the array's device address (cudaGetSymbolAddress, with that
- * device current); make that first call before any stream capture. Every call shares the one
+ * device current) and keeps it for the life of the process. Every call shares the one
  * array and leaves its contents behind; nothing in it needs to start at zero, since each call
  * writes all of the scratch it reads. Calls whose work overlaps on the GPU (different streams,
  * or host threads) race on the array: serialise them.
