@@ -461,6 +461,24 @@ def time_graph(fn, flush, steps, warmup):
     return statistics.mean(a.elapsed_time(b) for a, b in ev)
 
 
+def time_launches(launch, flush, steps, warmup):
+    """Mean ms of launch() (one graph launch the library owns) with L2 flushed before each."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        launch()
+    ev = []
+    for _ in range(steps):
+        flush.zero_()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        launch()
+        b.record()
+        ev.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.mean(a.elapsed_time(b) for a, b in ev)
+
+
 def run_layers(eg, desc, tables, geom, flush, peaks, n_layers=4, steps=20, warmup=3):
     """Stages 1 + 2 for several Engram layers: n_layers layers (each with its own hash constants
     and a 0.8-1.1 GB fp8 table) hashed and gathered by one engram_hash_rows_layers launch, against
@@ -551,7 +569,11 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
     def step():
         eg.engram_forward(desc, tables, weights, x, tok, cache, cache_len, None, out, ws)
 
-    ms = time_graph(step, flush, args.steps, args.warmup)
+    # the decode loop as a serving loop runs it: the library's own graph of the step
+    # (engram_forward_graph_create), one engram_graph_launch per step
+    graph = eg.EngramGraph(desc, tables, weights, x, tok, cache, cache_len, None, out, ws)
+    ms = time_launches(graph.launch, flush, args.steps, args.warmup)
+    graph.destroy()
     in_graph_ms = time_steps_in_graph(step, flush, 8)
     if eg.engram_check_errors() != 0:
         raise RuntimeError("device error word set during decode")
@@ -562,8 +584,9 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
            "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peaks["hbm_gbs"],
                         "unit": "GB/s", "frac": round(gbs / peaks["hbm_gbs"], 4),
                         "algorithmic_bytes": bytes_step},
-           "gpu_launches_per_step": 3, "timing": "CUDA graph replay per step, L2 flushed "
-                                                 "(256 MB write) before each"}
+           "gpu_launches_per_step": 3,
+           "timing": "engram_graph_launch per step (the library's CUDA graph of engram_forward: "
+                     "3 kernels), L2 flushed (256 MB write) before each"}
     # What the weight stream alone costs in this setting: the step's projection kernel by itself
     # (engram_wkv on the step's gathered rows: weight stream and kv stores, no hash and no
     # gate), after the same flush. The flush leaves L2 full of dirty lines, so every line the

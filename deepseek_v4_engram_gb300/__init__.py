@@ -3,7 +3,7 @@
 Importing the package loads nothing; the library is loaded on the first call and must have been
 built (``python -m deepseek_v4_engram_gb300.build``). There is no CPU fallback.
 """
-from .api import (DeviceLayerHash, DeviceTables, DeviceWeights, EngramError,  # noqa: F401
+from .api import (DeviceLayerHash, DeviceTables, DeviceWeights, EngramError, EngramGraph,  # noqa: F401,E501
                   engram_check_errors, engram_embed_rows, engram_embed_rows_shard,
                   engram_forward, engram_forward_ids,
                   engram_forward_noalloc,

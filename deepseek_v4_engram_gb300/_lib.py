@@ -67,6 +67,11 @@ SIGNATURES = {
     "engram_embed_rows": (ctypes.c_int, [_DESC, _P, _P, _P, _I64, _P, _P]),
     "engram_embed_rows_shard": (ctypes.c_int, [_DESC, _P, _P, _I64, _I64, _P, _I64, _P, _P]),
     "engram_probe_stream_read": (ctypes.c_int, [_P, _SZ, _I32, _P]),
+    "engram_forward_graph_create": (ctypes.c_int, [_DESC, _TAB, _WTS, _P, _P, _I32, _I32, _P, _P,
+                                                   _I32, _P, _P, _P, _P, _P, _P, _SZ,
+                                                   ctypes.POINTER(ctypes.c_void_p)]),
+    "engram_graph_launch": (ctypes.c_int, [_P, _P]),
+    "engram_graph_destroy": (ctypes.c_int, [_P]),
     "engram_wkv": (ctypes.c_int, [_P, _P, _P, _I64, _I32, _I32, _P]),
     "engram_gate_and_add": (ctypes.c_int, [_DESC, _P, _P, _P, _P, _P, _P, _P, _I64, _P]),
     "engram_wkv_gate_workspace_size": (_SZ, [_DESC, _I64]),

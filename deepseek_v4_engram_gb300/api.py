@@ -224,6 +224,46 @@ def engram_forward(desc, tables: DeviceTables, weights: DeviceWeights, x, tokens
         _stream(stream)))
 
 
+class EngramGraph:
+    """engram_forward captured once as a library-owned CUDA graph (engram_forward_graph_create);
+    launch() replays it. The tensors given at creation are kept referenced: refill x and tokens
+    in place between launches."""
+
+    def __init__(self, desc, tables: DeviceTables, weights: DeviceWeights, x, tokens, cache,
+                 cache_len, token_mask, out, workspace, hash_ids_out=None, gate_out=None,
+                 kv_out=None):
+        B, T = tokens.shape
+        handle = ctypes.c_void_p()
+        _check(lib().engram_forward_graph_create(
+            ctypes.byref(desc), ctypes.byref(tables.c), ctypes.byref(weights.c),
+            _ptr(x, "bf16", "x"), _ptr(tokens, "i32", "tokens"), B, T,
+            _ptr(cache, "i32", "cache"), _ptr(cache_len, "i32", "cache_len"), cache.shape[1],
+            _ptr(token_mask, "u8", "token_mask"), _ptr(out, "bf16", "out"),
+            _ptr(hash_ids_out, "i32", "hash_ids_out"), _ptr(gate_out, "f32", "gate_out"),
+            _ptr(kv_out, "bf16", "kv_out"), _ptr(workspace, "u8", "workspace"),
+            workspace.numel(), ctypes.byref(handle)))
+        self._handle = handle
+        self._keep = (desc, tables, weights, x, tokens, cache, cache_len, token_mask, out,
+                      workspace, hash_ids_out, gate_out, kv_out)
+
+    def launch(self, stream=None):
+        if not self._handle:
+            raise EngramError(_lib.ENGRAM_EINVAL, "graph destroyed")
+        _check(lib().engram_graph_launch(self._handle, _stream(stream)))
+
+    def destroy(self):
+        if self._handle:
+            lib().engram_graph_destroy(self._handle)
+            self._handle = ctypes.c_void_p()
+            self._keep = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
 def engram_forward_ids(desc, weights: DeviceWeights, x, hash_ids, token_mask, out, workspace,
                        gate_out=None, kv_out=None, stream=None):
     """Stages 2-4 from given hash ids [M, n_hash_cols] (the listing's forward(x, hash_ids, mask))."""

@@ -18,7 +18,7 @@ LIB = os.path.join(PKG, "libengram.so")
 INCLUDE = os.path.join(os.path.dirname(PKG), "include")
 SOURCES = ["capi.cu", "stages.cu", "wkv_sm103.cu", "small_m_sm103.cu", "forward_sm103.cu",
            "decode_sm103.cu", "noalloc.cu", "shard_rows.cu",
-           "stream_probe.cu"]
+           "stream_probe.cu", "graph.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC,-fvisibility=hidden",
          "--expt-relaxed-constexpr", f"-I{INCLUDE}"]

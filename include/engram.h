@@ -372,6 +372,34 @@ ENGRAM_API int engram_forward_noalloc(const engram_desc_t* desc, const engram_ta
                                       void* stream);
 
 /*
+ * The whole forward of engram_forward as one CUDA graph that the library builds and owns, for
+ * loops that run the same step shape again and again (decode: B sequences, T = 1 each step).
+ * engram_forward_graph_create takes engram_forward's arguments (without the stream), validates
+ * them as engram_forward does, captures engram_forward's kernel chain on a private stream (no
+ * kernel runs at creation) and instantiates it; *graph_out receives the handle, NULL on error.
+ * engram_graph_launch replays it on `stream` (one graph launch: the hash + gather, projection
+ * and gate kernels with their programmatic dependent launches), exactly as one engram_forward
+ * call with the creation's arguments would run. Every pointer given at creation is baked in:
+ * refill x, tokens and token_mask in place before each launch; the cache and cache_len advance
+ * on the device with every launch, as with consecutive engram_forward calls; out, gate_out,
+ * hash_ids_out, kv_out and the workspace are rewritten by every launch. Launches of one graph
+ * must not overlap each other or other work on the same buffers (they share the workspace).
+ * The graph belongs to the device current at creation; launching it with another device current
+ * returns ENGRAM_EINVAL. engram_graph_destroy frees it (NULL is allowed); destroy it before the
+ * buffers it names are freed. Errors: as engram_forward; a failed capture or instantiation
+ * returns ENGRAM_ECUDA.
+ */
+typedef struct engram_graph engram_graph_t;
+ENGRAM_API int engram_forward_graph_create(
+    const engram_desc_t* desc, const engram_tables_t* tables, const engram_weights_t* weights,
+    const uint16_t* x, const int32_t* tokens, int32_t B, int32_t T, int32_t* cache,
+    int32_t* cache_len, int32_t capacity, const uint8_t* token_mask, uint16_t* out,
+    int32_t* hash_ids_out, float* gate_out, uint16_t* kv_out, void* workspace,
+    size_t workspace_bytes, engram_graph_t** graph_out);
+ENGRAM_API int engram_graph_launch(const engram_graph_t* graph, void* stream);
+ENGRAM_API int engram_graph_destroy(engram_graph_t* graph);
+
+/*
  * A measurement call, not a stage of the forward (it has no counterpart on the pages): one read of
  * the device buffer src[0, bytes) spread evenly over every SM, discarding the bytes. Its duration
  * bounds from below any kernel that streams the same buffer once from the same memory state (the

@@ -83,6 +83,19 @@ def test_stream_probe_validation(lib):
     assert f(None, 0, 0, None) == _lib.ENGRAM_OK               # nothing to read
 
 
+def test_graph_handle_validation(lib):
+    d = desc()
+    t = _lib.EngramTables(0x1000, 1000, 0, 0x2000, 0x3000, 0x4000)
+    w = _lib.EngramWeights()
+    # no place for the handle: rejected before any CUDA call
+    assert lib.engram_forward_graph_create(ctypes.byref(d), ctypes.byref(t), ctypes.byref(w), 16,
+                                           16, 1, 1, 16, 16, 8, None, 16, None, None, None, 256,
+                                           1 << 20, None) == _lib.ENGRAM_EINVAL
+    assert lib.engram_graph_launch(None, None) == _lib.ENGRAM_EINVAL
+    assert b"graph" in lib.engram_last_error()
+    assert lib.engram_graph_destroy(None) == _lib.ENGRAM_OK
+
+
 def test_gate_rejects_aliasing_and_misalignment(lib):
     d = desc()
     x = 0x10000
