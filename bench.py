@@ -642,6 +642,28 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
                      "unit": "GB/s", "frac": round(gbs_ids / peaks["hbm_gbs"], 4),
                      "algorithmic_bytes": bytes_step},
         "timing": "CUDA graph replay per step, L2 flushed (256 MB write) before each"}
+    # Stages 3-4 from rows already gathered (a model step whose engram_hash_rows_layers launch has
+    # gathered every Engram layer's rows): the projection (engram_wkv) and the gate
+    # (engram_gate_and_add) of one layer.
+    kv_rows = torch.empty((B, geom.N), dtype=torch.int16, device="cuda")
+
+    def rows_step():
+        eg.engram_wkv(rows, weights.wkv, kv_rows)
+        eg.engram_gate_and_add(desc, x3, kv_rows, weights.q_weight, weights.k_weight, None, out3)
+
+    rows_ms = time_graph(rows_step, flush, args.steps, args.warmup)
+    if eg.engram_check_errors() != 0:
+        raise RuntimeError("device error word set during decode from rows")
+    gbs_rows = bytes_step / (rows_ms / 1e3) / 1e9
+    res["from_rows"] = {
+        "workload": f"decode B{B} x 1 token from rows already gathered (engram_wkv + "
+                    "engram_gate_and_add: projection, gate)",
+        "value": round(B / (rows_ms / 1e3), 1), "unit": "tokens/s",
+        "us_per_step": round(rows_ms * 1e3, 2),
+        "roofline": {"bound": "hbm", "achieved": round(gbs_rows, 1), "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": round(gbs_rows / peaks["hbm_gbs"], 4),
+                     "algorithmic_bytes": bytes_step},
+        "timing": "CUDA graph replay per step, L2 flushed (256 MB write) before each"}
     if in_graph_ms is not None:
         # the same steps without a graph launch per step: what a serving loop that captures many
         # layers or steps in one graph sees
