@@ -149,14 +149,15 @@ def test_forward_unfused_geometry(odd, B, T):
 
 @pytest.mark.parametrize("ws_mode", ["fastest", "kv", "min"])
 @pytest.mark.parametrize("B,T,mask_frac", [(1, 1, 0.0), (2, 77, 0.0), (1, 300, 0.1),
-                                           (4, 160, 0.1), (64, 1, 0.0), (1, 700, 0.1)])
+                                           (4, 160, 0.1), (64, 1, 0.0), (1, 513, 0.1),
+                                           (1, 700, 0.1)])
 def test_forward_full_width(wide, B, T, mask_frac, ws_mode):
     batch = synth.make_batch(wide.geom, B, T, synth.BASE_SEED + 200 + T, x_dist="student_t3",
                              mask_frac=mask_frac)
     check_against_oracle(wide, batch, run_forward(wide, batch, ws_mode=ws_mode))
 
 
-@pytest.mark.parametrize("B,T", [(1, 512), (1, 700), (2, 1024)])
+@pytest.mark.parametrize("B,T", [(1, 512), (1, 513), (1, 700), (2, 1024)])
 def test_deferred_output_equals_fused(wide, B, T):
     # from 512 to 2048 tokens the fastest workspace runs the fused kernel with its output deferred
     # (bf16 value rows, then out = x + gate * value in a second kernel); the minimum workspace runs
