@@ -49,11 +49,9 @@ constexpr int kEpiThreads = kEpiWarps * 32;
 constexpr int kXWarp = 2 + kEpiWarps;
 constexpr int kGateWarp = kXWarp + 1;
 constexpr int kFusedThreads = (kGateWarp + 1) * 32;
-constexpr int kFusedStages = 5;            // A/B ring depth
 constexpr int kPairB = kBN / 2;            // wkv rows of a key tile staged by each CTA of a pair
 constexpr int kStageABytes = kBM * kBK * 2;
 constexpr int kStageBBytes = kPairB * kBK * 2;
-constexpr int kXSlots = 4;                 // x ring depth
 constexpr int kXCols = 64;                 // columns per x box (128 B per row: one swizzle row)
 constexpr int kXBoxBytes = kBM * kXCols * 2;
 constexpr int kItemSlots = 4;              // item ring depth
@@ -65,13 +63,27 @@ constexpr int kMaxFusedDim = 5120;
 constexpr int kTokensPerTile = 2 * kBM;    // tokens per item
 constexpr uint32_t kEpiBarrier = 1;        // named barrier of the epilogue warps
 
+// Depths of the two shared-memory rings: operand stages (A and B of the pair MMA) and x slots.
+// With the gate in the epilogue, value items stream x in and out through the x slots; with the
+// output deferred only key items read x, and the same shared memory holds one more operand stage
+// (measured 3% faster at 512-2048 tokens, where the operand loads wait on HBM).
+struct RingsFused {
+  static constexpr int kStages = 5;
+  static constexpr int kXSlots = 4;
+};
+struct RingsDeferred {
+  static constexpr int kStages = 6;
+  static constexpr int kXSlots = 2;
+};
+
+template <class R>
 struct FusedShared {
-  uint64_t full[kFusedStages];    // even CTA: operands of both CTAs landed
-  uint64_t empty[kFusedStages];   // both CTAs: the pair MMAs are done with the stage
+  uint64_t full[R::kStages];      // even CTA: operands of both CTAs landed
+  uint64_t empty[R::kStages];     // both CTAs: the pair MMAs are done with the stage
   uint64_t tfull[2];              // both CTAs: accumulator ready
   uint64_t tempty[2];             // even CTA: both CTAs' epilogues released the accumulator
-  uint64_t xfull[kXSlots];
-  uint64_t xempty[kXSlots];
+  uint64_t xfull[R::kXSlots];
+  uint64_t xempty[R::kXSlots];
   uint64_t ifull[kItemSlots];     // both CTAs: item index written (by the even CTA's producer)
   uint64_t iempty[kItemSlots];    // even CTA: every reader of both CTAs has read the slot
   uint64_t pfull[2];              // a key tile's partial sums are in global memory (128 arrivals)
@@ -85,11 +97,13 @@ struct FusedShared {
   float part[3][kBM];
 };
 
-constexpr size_t kFusedSmemBytes = size_t(kFusedStages) * (kStageABytes + kStageBBytes) +
-                                   size_t(kXSlots) * kXBoxBytes + sizeof(FusedShared) + 1024;
-static_assert(kFusedSmemBytes <= 232448, "fused kernel exceeds 227 KB of shared memory");
-
-size_t fused_smem_bytes() { return kFusedSmemBytes; }
+template <class R>
+constexpr size_t fused_smem_bytes() {
+  return size_t(R::kStages) * (kStageABytes + kStageBBytes) + size_t(R::kXSlots) * kXBoxBytes +
+         sizeof(FusedShared<R>) + 1024;
+}
+static_assert(fused_smem_bytes<RingsFused>() <= 232448, "fused kernel exceeds 227 KB");
+static_assert(fused_smem_bytes<RingsDeferred>() <= 232448, "fused kernel exceeds 227 KB");
 
 struct FusedParams {
   const uint16_t* q;
@@ -149,10 +163,11 @@ __device__ __forceinline__ void write_x_half_row(uint8_t* box, int row, int half
 
 // Consumer side of the x ring. release() hands a slot back to the x producer: the proxy fence
 // orders this thread's reads of the slot before the TMA load that will overwrite it.
+template <int kSlots>
 struct XRing {
   uint32_t slot = 0, phase = 0;
   __device__ __forceinline__ void advance() {
-    if (++slot == kXSlots) {
+    if (++slot == kSlots) {
       slot = 0;
       phase ^= 1u;
     }
@@ -222,7 +237,8 @@ __device__ __forceinline__ int32_t atom_add_acq_rel_gpu(int32_t* p, int32_t v) {
 // tells the even CTA's producer that this reader is done with the slot.
 struct ItemReader {
   uint32_t slot = 0, phase = 0;
-  __device__ __forceinline__ bool next(FusedShared* sh, int32_t& item, volatile int* abort,
+  template <class Sh>
+  __device__ __forceinline__ bool next(Sh* sh, int32_t& item, volatile int* abort,
                                        uint32_t* err) {
     if (!mbar_wait<true>(&sh->ifull[slot], phase, abort, err)) return false;
     item = *reinterpret_cast<volatile int32_t*>(&sh->item[slot]);
@@ -245,6 +261,7 @@ __device__ __forceinline__ int32_t wkv_tile(const FusedItem& it, int32_t key_til
   return it.value ? key_tiles + it.col : it.col;
 }
 
+template <class R>
 __global__ void __launch_bounds__(kFusedThreads, 1)
     engram_fused_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmW,
@@ -253,9 +270,11 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align_1024(smem_raw);
   uint8_t* sA = smem;
+  constexpr int kFusedStages = R::kStages;
+  constexpr int kXSlots = R::kXSlots;
   uint8_t* sB = sA + kFusedStages * kStageABytes;
   uint8_t* sX = sB + kFusedStages * kStageBBytes;
-  FusedShared* sh = reinterpret_cast<FusedShared*>(sX + kXSlots * kXBoxBytes);
+  FusedShared<R>* sh = reinterpret_cast<FusedShared<R>*>(sX + kXSlots * kXBoxBytes);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int32_t half_m = static_cast<int32_t>(cluster_ctarank());   // which 128 tokens
@@ -504,7 +523,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quad * 32) << 16;
     const int64_t N = static_cast<int64_t>(dim) * (hc + 1);
     const uint32_t tempty_leader0 = map_to_rank(smem_u32(&sh->tempty[0]), 0);
-    XRing xr;
+    XRing<kXSlots> xr;
     ItemReader ir;
     uint32_t nkey = 0;
     int32_t pending = -1;   // thread 64: x slot whose TMA store may still be reading it
@@ -609,7 +628,8 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             vb[e] = pack_bf16x2(__uint_as_float(r[2 * e]), __uint_as_float(r[2 * e + 1]));
           if (valid) {
             store_words<16>(p.vout + m * dim + colb, vb);
-            if (p.kv_out) store_words<16>(p.kv_out + m * N + static_cast<int64_t>(hc) * dim + colb, vb);
+            if (p.kv_out)
+              store_words<16>(p.kv_out + m * N + static_cast<int64_t>(hc) * dim + colb, vb);
           }
         }
       } else {
@@ -719,7 +739,7 @@ int query_resident_pairs() {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2, 1, 1);
   cfg.blockDim = dim3(kFusedThreads, 1, 1);
-  cfg.dynamicSmemBytes = fused_smem_bytes();
+  cfg.dynamicSmemBytes = fused_smem_bytes<RingsFused>();
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
@@ -728,7 +748,8 @@ int query_resident_pairs() {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, engram_fused_kernel, &cfg) != cudaSuccess || n <= 0)
+  if (cudaOccupancyMaxActiveClusters(&n, engram_fused_kernel<RingsFused>, &cfg) != cudaSuccess ||
+      n <= 0)
     n = 1;
   return n;
 }
@@ -785,9 +806,18 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl) {
       !tensor_map_3d_bf16(&tmX, a.x, a.dim, a.hc, a.M, kXCols, 1, kBM) ||
       !tensor_map_3d_bf16(&tmOut, a.out, a.dim, a.hc, a.M, kXCols, 1, kBM))
     return cudaErrorInvalidValue;
+  // the deferred output (value rows stored, no x for value items) takes the deeper operand ring
+  const bool deferred = a.vout != nullptr;
+  const void* kernel = deferred
+                           ? reinterpret_cast<const void*>(engram_fused_kernel<RingsDeferred>)
+                           : reinterpret_cast<const void*>(engram_fused_kernel<RingsFused>);
+  const size_t smem = deferred ? fused_smem_bytes<RingsDeferred>() : fused_smem_bytes<RingsFused>();
   {
-    const cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(engram_fused_kernel),
-                                              fused_smem_bytes());
+    // the resident-pairs query below runs on the fused-output kernel: raise its limit in any case
+    cudaError_t e = ensure_dynamic_smem(
+        reinterpret_cast<const void*>(engram_fused_kernel<RingsFused>),
+        fused_smem_bytes<RingsFused>());
+    if (e == cudaSuccess && deferred) e = ensure_dynamic_smem(kernel, smem);
     if (e != cudaSuccess) return e;
   }
   const ScratchLayout l = scratch_layout(a.M, a.hc, a.dim);
@@ -829,7 +859,7 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(2, static_cast<unsigned>(pairs), 1);
   cfg.blockDim = dim3(kFusedThreads, 1, 1);
-  cfg.dynamicSmemBytes = fused_smem_bytes();
+  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   // No co-residency is needed: a pair takes items only while it runs, and takes them in the
   // schedule's order, so every item a value item waits for is held by a running pair.
@@ -844,7 +874,9 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t st, bool pdl) {
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = (pdl && a.sync_cleared) ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, engram_fused_kernel, tmA, tmW, tmX, tmOut, p);
+  if (deferred)
+    return cudaLaunchKernelEx(&cfg, engram_fused_kernel<RingsDeferred>, tmA, tmW, tmX, tmOut, p);
+  return cudaLaunchKernelEx(&cfg, engram_fused_kernel<RingsFused>, tmA, tmW, tmX, tmOut, p);
 }
 
 }  // namespace engram
