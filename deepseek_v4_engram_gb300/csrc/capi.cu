@@ -183,11 +183,13 @@ struct Plan {
   size_t bytes;
 };
 constexpr int64_t kFusedMinTokens = 640;
-// the deferred-output fused plan's range, measured on one GPU against the other plans (A/B):
-// 65.6 vs 70.0 us at 512 tokens, 96.7 vs 105.3 at 1024, 150.8 vs 157.6 at 2048; slower at 384
-// (63.8 vs 58.0) and at 4096 (281 vs 266)
-constexpr int64_t kDeferredMinTokens = 512;
-constexpr int64_t kDeferredMaxTokens = 2048;
+// Where the deferred-output fused plan is the fastest, measured on one GPU against the other
+// plans (whole engram_forward, B1): one nearly full token tile, 51.2-51.8 vs 54.0-54.1 us at 256
+// tokens (54.0 vs 53.9 at 240: the small-batch plan grows with M, the fused kernel's one tile
+// does not); and 512 to 2048 tokens, 63.2 vs 70.0 at 512, 96.1 vs 105.3 at 1024, 145.7 vs 157.6
+// at 2048. Slower at 288-384 (61.4 vs 54.0 at 288: a second, nearly empty tile) and from 3072
+// (213.7 vs 205.9; 272.7 vs 266.3 at 4096).
+bool deferred_plan_wins(int64_t M) { return (M >= 240 && M <= 256) || (M >= 512 && M <= 2048); }
 constexpr int kMaxPlans = 6;
 
 // Candidate plans in order of preference; returns how many were written.
@@ -200,7 +202,7 @@ int forward_plans(const engram_desc_t* d, int64_t M, Plan* out) {
   const bool fused = fused_supported(K, d->hc_mult, d->dim);
   int n = 0;
   if (decode_supported(M, N, K)) out[n++] = {Path::kDecode, 1, base + kv_bytes};
-  if (fused && M >= kDeferredMinTokens && M <= kDeferredMaxTokens)
+  if (fused && deferred_plan_wins(M))
     out[n++] = {Path::kFusedDeferred, 1,
                 base + round256(fused_scratch_bytes(M, d->hc_mult, d->dim)) +
                     round256(size_t(M) * d->dim * 2)};

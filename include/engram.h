@@ -308,12 +308,12 @@ ENGRAM_API size_t engram_forward_workspace_size(const engram_desc_t* desc, int64
  * How stages 3 and 4 run depends on M and on the workspace given (the fastest path that fits):
  * up to 256 tokens, a weight-streaming projection over every SM (for up to 64 tokens, a fixed
  * share of the weight rows per SM) into a bf16 kv, then the gate kernel; below 512 tokens, the
- * persistent projection GEMM into a bf16 kv then the gate kernel; from 512 to 2048 tokens, the
- * fused projection kernel with its output deferred (it computes the gates and stores the bf16
- * value rows; a second kernel then writes out = x + gate * value), bit for bit what the fused
- * kernel gives; above 2048 tokens, or when only the minimum workspace is given, the projection
- * with the gate fused into its epilogue (as engram_wkv_gate). Every path runs on the GPU;
- * results agree within the projection's f32-summation bound.
+ * persistent projection GEMM into a bf16 kv then the gate kernel; from 240 to 256 and from 512
+ * to 2048 tokens, the fused projection kernel with its output deferred (it computes the gates and
+ * stores the bf16 value rows; a second kernel then writes out = x + gate * value), bit for bit
+ * what the fused kernel gives; above 2048 tokens, or when only the minimum workspace is given,
+ * the projection with the gate fused into its epilogue (as engram_wkv_gate). Every path runs on
+ * the GPU; results agree within the projection's f32-summation bound.
  */
 ENGRAM_API int engram_forward(const engram_desc_t* desc, const engram_tables_t* tables,
                               const engram_weights_t* weights, const uint16_t* x,

@@ -157,9 +157,10 @@ def test_forward_full_width(wide, B, T, mask_frac, ws_mode):
     check_against_oracle(wide, batch, run_forward(wide, batch, ws_mode=ws_mode))
 
 
-@pytest.mark.parametrize("B,T", [(1, 512), (1, 513), (1, 700), (2, 1024)])
+@pytest.mark.parametrize("B,T", [(1, 256), (2, 125), (1, 512), (1, 513), (1, 700), (2, 1024)])
 def test_deferred_output_equals_fused(wide, B, T):
-    # from 512 to 2048 tokens the fastest workspace runs the fused kernel with its output deferred
+    # at 240-256 and 512-2048 tokens the fastest workspace runs the fused kernel with its output
+    # deferred
     # (bf16 value rows, then out = x + gate * value in a second kernel); the minimum workspace runs
     # the fused kernel alone. Both round the value to bf16 and take one fma per element: equal bits.
     batch = synth.make_batch(wide.geom, B, T, synth.BASE_SEED + 260 + T, x_dist="student_t3",
