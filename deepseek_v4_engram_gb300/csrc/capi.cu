@@ -170,7 +170,7 @@ constexpr size_t round256(size_t n) { return (n + 255) & ~size_t(255); }
 //  - kUnfused: the persistent projection GEMM into a bf16 kv, then the gate kernel; measured
 //              faster than the fused kernel below 640 tokens (too few items to fill the GPU
 //              past the fused kernel's cold start: 72 vs 74 us at 512, 86 vs 82 us at 640);
-//  - kFusedDeferred: 512 to 2048 tokens: the fused kernel with deferred output: its value
+//  - kFusedDeferred: 240-256 and 512-2048 tokens: the fused kernel with deferred output: its value
 //              tiles store bf16 value rows instead of waiting for the gates, and a light kernel
 //              then writes out = x + gate * value; for batches too small for the fused kernel to
 //              hide its value tiles' wait and x traffic behind the key tiles of other token
