@@ -270,8 +270,10 @@ def run_native(args):
         "kernel_timing": "engram_wkv_gate alone on the step's rows (CUDA graph replay: counter "
                          "memset + kernel), L2 flushed before each launch",
         "kernel_share_of_step": round(statistics.mean(kern_ms) / statistics.mean(step_ms), 4),
-        "traffic": (None if traffic is None else
-                    round(traffic["bytes_per_launch"] * M / traffic["tokens_per_launch"])),
+        # the captured bytes hold for the captured token count only (the weight's share of the
+        # traffic does not grow with the tokens)
+        "traffic": (None if traffic is None or traffic["tokens_per_launch"] != M else
+                    traffic["bytes_per_launch"]),
         "algorithmic_bytes": M * BYTES_PER_TOKEN + WKV_BYTES,
     }
     # whole-step roofline: max(FLOPs at bf16 peak, bytes at HBM peak)
