@@ -96,6 +96,19 @@ def test_graph_handle_validation(lib):
     assert lib.engram_graph_destroy(None) == _lib.ENGRAM_OK
 
 
+def test_forward_workspace_is_the_deferred_plans_exactly_in_its_ranges(lib):
+    # the fastest workspace holds the gathered rows, the fused kernel's scratch and the bf16 value
+    # rows exactly where engram_forward takes the deferred-output plan: 240-256 and 512-2048 tokens
+    # at the full geometry
+    d = desc(dim=5120, head_dim=64, num_embeddings=1 << 20)
+    r = lambda n: (n + 255) // 256 * 256
+    for M in (200, 239, 240, 250, 256, 257, 384, 511, 512, 700, 2048, 2049, 4096):
+        ws = lib.engram_forward_workspace_size(ctypes.byref(d), M)
+        deferred = (r(M * 1536 * 2) + r(lib.engram_wkv_gate_workspace_size(ctypes.byref(d), M))
+                    + r(M * 5120 * 2))
+        assert (ws == deferred) == (240 <= M <= 256 or 512 <= M <= 2048), M
+
+
 def test_gate_rejects_aliasing_and_misalignment(lib):
     d = desc()
     x = 0x10000
