@@ -171,6 +171,42 @@ def test_deferred_output_equals_fused(wide, B, T):
         np.testing.assert_array_equal(deferred[key], fused[key])
 
 
+# Other shapes the kernels take: 1, 2 and 8 streams, 256-768 columns per stream, 2-5-grams,
+# head_dim 32 and 64 (every projection path at each: decode, small-batch, deferred and fused)
+OTHER = {
+    "hc2_dim512": synth.Geometry(dim=512, hc_mult=2, n_heads=4, max_ngram_size=3, head_dim=32,
+                                 vocab=3000, n_compressed=1500, prime_floor=2003),
+    "hc8_dim256": synth.Geometry(dim=256, hc_mult=8, n_heads=8, max_ngram_size=4, head_dim=32,
+                                 vocab=3000, n_compressed=1500, prime_floor=3001),
+    "hc1_dim768": synth.Geometry(dim=768, hc_mult=1, n_heads=2, max_ngram_size=5, head_dim=64,
+                                 vocab=3000, n_compressed=1500, prime_floor=4001),
+}
+
+
+@pytest.fixture(scope="module")
+def others():
+    from tests.gpu_fixtures import DeviceModel
+    return {k: DeviceModel(synth.make_model(g, synth.BASE_SEED + 70 + i, scale_mode="pow2"))
+            for i, (k, g) in enumerate(OTHER.items())}
+
+
+@pytest.mark.parametrize("name", list(OTHER))
+@pytest.mark.parametrize("B,T", [(8, 1), (1, 200), (2, 125), (1, 600), (1, 2100)])
+def test_forward_other_geometries(others, name, B, T):
+    dm = others[name]
+    batch = synth.make_batch(dm.geom, B, T, synth.BASE_SEED + 280 + T, x_dist="student_t3",
+                             mask_frac=0.1 if T > 1 else 0.0)
+    r = run_forward(dm, batch)
+    check_against_oracle(dm, batch, r)
+    if B * T >= 200:   # and the fused kernel alone (the minimum workspace) gives the same bits as
+        fused = run_forward(dm, batch, ws_mode="min")   # the fastest plan where that is fused
+        if 240 <= B * T <= 256 or 512 <= B * T:
+            for key in ("out", "gate", "kv", "hash_ids"):
+                np.testing.assert_array_equal(r[key], fused[key])
+        else:
+            check_against_oracle(dm, batch, fused)
+
+
 def test_prefill_then_decode_equals_one_prefill(wide):
     # the look-back cache carries across calls: prefill(T) == prefill(T-j) + j decode steps
     B, T, j = 3, 40, 4
