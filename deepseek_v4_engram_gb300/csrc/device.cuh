@@ -336,6 +336,16 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, const void*
       "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z)
       : "memory");
 }
+// tma_store_3d with an L2 cache policy (from l2_evict_*_policy) for the written lines.
+__device__ __forceinline__ void tma_store_3d_hint(const CUtensorMap* map, const void* src,
+                                                  int32_t x, int32_t y, int32_t z,
+                                                  uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.global.shared::cta.bulk_group.L2::cache_hint"
+      " [%0, {%2, %3, %4}], [%1], %5;" ::"l"(reinterpret_cast<uint64_t>(map)),
+      "r"(smem_u32(src)), "r"(x), "r"(y), "r"(z), "l"(policy)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }

@@ -524,6 +524,9 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
     const int64_t N = static_cast<int64_t>(dim) * (hc + 1);
     const uint32_t tempty_leader0 = map_to_rank(smem_u32(&sh->tempty[0]), 0);
     XRing<kXSlots> xr;
+    // out is written once and read by nothing of this kernel: its lines go first (measured 0.5%
+    // faster at 4096 and 16384 tokens than the default policy)
+    const uint64_t out_l2 = l2_evict_first_policy();
     ItemReader ir;
     uint32_t nkey = 0;
     int32_t pending = -1;   // thread 64: x slot whose TMA store may still be reading it
@@ -670,7 +673,7 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
             const bool fail = epi_any(!ok);
             if (threadIdx.x == 64) {
               if (!fail) {
-                tma_store_3d(&tmOut, box, colb, s2, m0);
+                tma_store_3d_hint(&tmOut, box, colb, s2, m0, out_l2);
                 bulk_commit_group();
               }
               bulk_wait_group_read<1>();   // every store but this one has read its slot
