@@ -609,7 +609,7 @@ def run_decode(eg, desc, tables, weights, model, geom, args, flush, peaks, B=64,
     # (engram_probe_stream_read: bulk copies into the projection's ring depth, or plain loads),
     # after the same flush.
     floor = {}
-    for method, name in ((0, "bulk_copies"), (1, "plain_loads")):
+    for method, name in ((0, "bulk_copies"), (1, "plain_loads"), (2, "bulk_copies_evict_first")):
         f_ms = time_graph(lambda m=method: eg.api.engram_probe_stream_read(weights.wkv, m), flush,
                           args.steps, args.warmup)
         floor[name] = {"us": round(f_ms * 1e3, 2),

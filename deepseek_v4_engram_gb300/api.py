@@ -161,7 +161,8 @@ def engram_embed_rows_shard(desc, table_shard, scales_shard, row_begin: int, ids
 
 
 def engram_probe_stream_read(buf, method: int, stream=None):
-    """One read of `buf` (a contiguous CUDA tensor) over every SM: 0 bulk copies, 1 plain loads."""
+    """One read of `buf` (a contiguous CUDA tensor) over every SM: 0 bulk copies, 1 plain loads,
+    2 bulk copies with an L2 evict-first policy."""
     if not (isinstance(buf, torch.Tensor) and buf.is_cuda and buf.is_contiguous()):
         raise TypeError("buf: expected a contiguous CUDA tensor")
     _check(lib().engram_probe_stream_read(ctypes.c_void_p(buf.data_ptr()),

@@ -497,7 +497,8 @@ ENGRAM_API int engram_embed_rows_shard(const engram_desc_t* desc, const uint8_t*
 ENGRAM_API int engram_probe_stream_read(const void* src, size_t bytes, int32_t method,
                                         void* stream) {
   g_msg[0] = 0;
-  if (method != kProbeBulk && method != kProbePlain) return fail(ENGRAM_EINVAL, "bad method");
+  if (method != kProbeBulk && method != kProbePlain && method != kProbeBulkEvictFirst)
+    return fail(ENGRAM_EINVAL, "bad method");
   if (bytes % 16 != 0 || bytes >= (size_t(1) << 40))
     return fail(ENGRAM_EINVAL, "bytes must be a multiple of 16 below 2^40");
   if (bytes == 0) return ENGRAM_OK;

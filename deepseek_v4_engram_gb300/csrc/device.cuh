@@ -314,6 +314,16 @@ __device__ __forceinline__ void tma_load_2d_pair_hint(void* dst, const CUtensorM
       : "memory");
 }
 
+// tma_load_2d with an L2 cache policy (from l2_evict_*_policy).
+__device__ __forceinline__ void tma_load_2d_hint(void* dst, const CUtensorMap* map, uint64_t* bar,
+                                                 int32_t x, int32_t y, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
+      : "memory");
+}
+
 // tma_load_3d with an L2 cache policy.
 __device__ __forceinline__ void tma_load_3d_hint(void* dst, const CUtensorMap* map, uint64_t* bar,
                                                  int32_t x, int32_t y, int32_t z,

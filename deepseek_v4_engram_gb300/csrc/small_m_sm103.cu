@@ -90,6 +90,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
       // producer: a ring of S stages. The wkv slices do not depend on earlier kernels, so the
       // first stages' weight loads are issued before waiting for the kernel that wrote the
       // activations (with a programmatic launch that wait overlaps the previous kernel's tail).
+      // the weight is read once: evict-first, so that it replaces its own lines in L2
+      const uint64_t stream_l2 = l2_evict_first_policy();
       uint32_t stage = 0, phase = 0, issued_mask = 0, issued_parity = 0;
       int pre = 0;
       if (static_cast<int>(blockIdx.x) < items) {
@@ -98,7 +100,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         pre = kb_per < S ? kb_per : S;
         for (int j = 0; j < pre; ++j) {
           mbar_arrive_expect_tx(&sh->full[j], a_bytes + b_bytes);
-          tma_load_2d(smem + j * stage_bytes, &tmW, &sh->full[j], (kb0 + j) * kBK, n0);
+          tma_load_2d_hint(smem + j * stage_bytes, &tmW, &sh->full[j], (kb0 + j) * kBK, n0,
+                           stream_l2);
         }
       }
       pdl_wait();
@@ -113,7 +116,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
           if (g >= pre) {
             if (!mbar_wait(&sh->empty[stage], phase ^ 1u, abort, p.err)) { ok = false; break; }
             mbar_arrive_expect_tx(&sh->full[stage], a_bytes + b_bytes);
-            tma_load_2d(st, &tmW, &sh->full[stage], kb * kBK, n0);
+            tma_load_2d_hint(st, &tmW, &sh->full[stage], kb * kBK, n0, stream_l2);
           }
           tma_load_2d(st + a_bytes, &tmA, &sh->full[stage], kb * kBK, 0);
           issued_mask |= 1u << stage;

@@ -7,7 +7,9 @@
 //  - kBulk: as 32 KB bulk copies (cp.async.bulk) into a 6-stage shared-memory ring, one thread
 //    issuing, 192 KB in flight per SM as in the decode projection's ring; or
 //  - kPlain: as 16-byte non-caching loads by 512 threads, four per thread in flight, XOR-folded
-//    into one word per CTA so that the loads cannot be dropped.
+//    into one word per CTA so that the loads cannot be dropped;
+//  - kBulkEvictFirst: as kBulk, with an L2 evict-first policy on the copies (what the decode
+//    projection uses for the weight).
 #include "device.cuh"
 #include "kernels.h"
 #include "stream_probe.h"
@@ -35,6 +37,15 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t b
       : "memory");
 }
 
+__device__ __forceinline__ void bulk_load_hint(void* dst, const void* src, uint32_t bytes,
+                                               uint64_t* bar, uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+      " [%0], [%1], %2, [%3], %4;" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+
 // share of CTA b of n over `units` 16-byte units: [lo, hi)
 __device__ __forceinline__ void cta_share(int64_t units, int64_t& lo, int64_t& hi) {
   lo = units * blockIdx.x / gridDim.x;
@@ -42,7 +53,7 @@ __device__ __forceinline__ void cta_share(int64_t units, int64_t& lo, int64_t& h
 }
 
 __global__ void __launch_bounds__(32, 1) probe_bulk_kernel(const uint8_t* src, int64_t units,
-                                                           uint32_t* err) {
+                                                           int32_t evict_first, uint32_t* err) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = align_1024(smem_raw);
   ProbeShared* sh = reinterpret_cast<ProbeShared*>(ring + kProbeStages * kProbeChunk);
@@ -66,7 +77,11 @@ __global__ void __launch_bounds__(32, 1) probe_bulk_kernel(const uint8_t* src, i
     const int64_t left = bytes - c * kProbeChunk;
     const uint32_t n = static_cast<uint32_t>(left < kProbeChunk ? left : kProbeChunk);
     mbar_arrive_expect_tx(&sh->full[stage], n);
-    bulk_load(ring + stage * kProbeChunk, p + c * kProbeChunk, n, &sh->full[stage]);
+    if (evict_first)
+      bulk_load_hint(ring + stage * kProbeChunk, p + c * kProbeChunk, n, &sh->full[stage],
+                     l2_evict_first_policy());
+    else
+      bulk_load(ring + stage * kProbeChunk, p + c * kProbeChunk, n, &sh->full[stage]);
     issued = c + 1;
   }
   // every copy issued has landed before the CTA exits (each stage's last fill; bounded)
@@ -117,11 +132,12 @@ cudaError_t launch_stream_probe(const void* src, int64_t bytes, int32_t method, 
                                 cudaStream_t st) {
   const int64_t units = bytes / 16;
   const unsigned grid = static_cast<unsigned>(device_sm_count());
-  if (method == kProbeBulk) {
+  if (method == kProbeBulk || method == kProbeBulkEvictFirst) {
     const size_t smem = probe_bulk_smem_bytes();
     cudaError_t e = ensure_dynamic_smem(reinterpret_cast<const void*>(probe_bulk_kernel), smem);
     if (e != cudaSuccess) return e;
-    probe_bulk_kernel<<<grid, 32, smem, st>>>(static_cast<const uint8_t*>(src), units, err);
+    probe_bulk_kernel<<<grid, 32, smem, st>>>(static_cast<const uint8_t*>(src), units,
+                                              method == kProbeBulkEvictFirst, err);
   } else {
     probe_plain_kernel<<<grid, kPlainThreads, 0, st>>>(static_cast<const uint8_t*>(src), units);
   }

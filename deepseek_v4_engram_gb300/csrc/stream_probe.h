@@ -7,7 +7,7 @@
 
 namespace engram {
 
-enum : int32_t { kProbeBulk = 0, kProbePlain = 1 };
+enum : int32_t { kProbeBulk = 0, kProbePlain = 1, kProbeBulkEvictFirst = 2 };
 
 cudaError_t launch_stream_probe(const void* src, int64_t bytes, int32_t method, uint32_t* err,
                                 cudaStream_t st);

@@ -406,7 +406,8 @@ ENGRAM_API int engram_graph_destroy(engram_graph_t* graph);
  * decode projection streams the wkv weight once per step), whatever that kernel computes.
  *   method 0: 32 KB bulk copies (cp.async.bulk) into a 6-stage shared-memory ring per SM (the
  *             decode projection's bytes in flight); method 1: 16-byte non-caching loads, 512
- *             threads per SM, four loads in flight per thread.
+ *             threads per SM, four loads in flight per thread; method 2: as method 0, with an L2
+ *             evict-first policy on the copies (the decode projection's policy for the weight).
  * src must be 16-byte aligned and bytes a multiple of 16 (else ENGRAM_EINVAL); bytes = 0 launches
  * nothing. Writes nothing the caller can see.
  */

@@ -76,7 +76,7 @@ def test_shard_rows_validation(lib):
 
 def test_stream_probe_validation(lib):
     f = lib.engram_probe_stream_read
-    assert f(16, 64, 2, None) == _lib.ENGRAM_EINVAL            # no such method
+    assert f(16, 64, 3, None) == _lib.ENGRAM_EINVAL            # no such method
     assert f(16, 40, 0, None) == _lib.ENGRAM_EINVAL            # not a multiple of 16 bytes
     assert f(24, 64, 1, None) == _lib.ENGRAM_EINVAL            # misaligned
     assert f(None, 64, 0, None) == _lib.ENGRAM_EINVAL

@@ -223,7 +223,7 @@ def test_gate_zero_key_and_tiny(tiny):
 def test_stream_probe_reads_without_error(nbytes):
     # the measurement call: every share of the buffer read, every wait completed in time
     buf = torch.empty(nbytes // 4, dtype=torch.int32, device="cuda").fill_(7)
-    for method in (0, 1):
+    for method in (0, 1, 2):
         eg.api.engram_probe_stream_read(buf, method)
     torch.cuda.synchronize()
     assert eg.engram_check_errors() == 0
