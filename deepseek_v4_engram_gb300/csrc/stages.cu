@@ -196,13 +196,14 @@ __global__ void __launch_bounds__(kHrThreads)
     const uint4* src =
         reinterpret_cast<const uint4*>(L.table + static_cast<int64_t>(id) * a.head_dim);
     const uint8_t* sc = L.scales + static_cast<int64_t>(id) * (a.head_dim / 32);
+    const uint64_t once = l2_evict_first_policy();
     if (chunks == 4) {   // head_dim 64: all four loads in flight at once
       uint4 code[4];
       uint32_t scl[2];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) code[c] = __ldg(src + c);
-      scl[0] = __ldg(sc);
-      scl[1] = __ldg(sc + 1);
+      for (int c = 0; c < 4; ++c) code[c] = ldg_hint(src + c, once);
+      scl[0] = ldg_u8_hint(sc, once);
+      scl[1] = ldg_u8_hint(sc + 1, once);
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint4 lo, hi;
@@ -213,7 +214,7 @@ __global__ void __launch_bounds__(kHrThreads)
     } else {
       for (int32_t c = 0; c < chunks; ++c) {
         uint4 lo, hi;
-        dequant16(__ldg(src + c), e8m0_to_f32(__ldg(sc + c / 2)), lo, hi);
+        dequant16(ldg_hint(src + c, once), e8m0_to_f32(ldg_u8_hint(sc + c / 2, once)), lo, hi);
         dst[2 * c] = lo;
         dst[2 * c + 1] = hi;
       }
